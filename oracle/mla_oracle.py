@@ -1,0 +1,290 @@
+"""Plain fp64 CPU oracle of the MLA paged decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module; the library
+(``mla_decode_paged_gb300``) never does, and this module imports nothing from
+it.  Inputs are numpy arrays of raw codes (uint8 fp8 codes, uint16 bf16
+bits, int32 indices); every value is widened to float64 by the decoders
+below, and every step is the plain definition, written out with no blocking,
+fusion or reordering beyond it.
+
+What the path computes, per request r, query row t (r*qlen <= t <
+(r+1)*qlen) and real head h < H (vLLM API page
+``vllm.models.kimi_k3.amd.specialized_decode.runtime.mla``, functions
+``m1c_inputs`` and ``attend``; page
+``vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value``, classes
+``MlaValue`` and ``MlaGate``):
+
+    K_j          = e4m3fn(kv[pages[indptr[r] + j]]) * kv_scale,  j < L_r
+    s_j          = scale * <q[t, h, :576], K_j[:576]>
+    lse[t, h]    = ln sum_j exp(s_j)                  (-inf when L_r == 0)
+    latent[t, h] = sum_j exp(s_j - lse) * K_j[:512]   (0 when L_r == 0)
+    val[t, h, v] = sum_c latent[t, h, c] * W_UV[h, v, c]
+    out[t, h*128 + v] = val * sigmoid(gate[t, h*128 + v])  if L_r > 0 else 0
+
+Readings where the pages are silent (each one is listed with its reason in
+the design notes): no intra-request causal mask; natural-log LSE of the
+scaled scores; ``kv_scale`` multiplies the stored fp8 value and applies to
+both the score K and the value V; OCP e4m3fn; page size 1; the split plan
+of :func:`split_plan`; the gate is raw logits and the sigmoid is exact.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+D_QK = 576
+D_LATENT = 512
+D_V = 128
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def e4m3fn_to_f64(codes) -> np.ndarray:
+    """Decode OCP FP8 E4M3 ("e4m3fn") bytes to float64.
+
+    The cache is read through ``current_platform.fp8_dtype()`` (``attend`` and
+    ``m1c_inputs``: ``kv_cache.view(fp8)``); on this GPU that is OCP E4M3:
+    1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, subnormals when
+    the exponent field is 0, NaN for S.1111.111, no infinities.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    subnormal = sign * np.ldexp(m / 8.0, -6)
+    out = np.where(e == 0, subnormal, normal)
+    out = np.where((e == 15) & ((c & 7) == 7), np.nan, out)
+    return out.astype(np.float64)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Widen bfloat16 bit patterns (uint16) to float64: a bf16 is the top half
+    of an IEEE binary32, so the widening is exact."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def sigmoid(x) -> np.ndarray:
+    """The logistic function 1 / (1 + exp(-x)), in float64.  ``MlaGate`` and
+    ``MlaValue`` apply it to the raw gate inside the kernel."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-x))
+
+
+# ---------------------------------------------------------------------------
+# Paged gather
+# ---------------------------------------------------------------------------
+
+def gather_rows(kv_codes, pages, indptr, r: int) -> np.ndarray:
+    """Request r's KV rows, as raw fp8 codes [L_r, 576]: the flat token rows
+    ``kv.view(-1, 576)`` addressed by ``pages[indptr[r]:indptr[r+1]]``
+    (``m1c_inputs``: ``kv``, ``pages``, ``indptr``; page size 1)."""
+    kv_codes = np.asarray(kv_codes, dtype=np.uint8)
+    lo, hi = int(indptr[r]), int(indptr[r + 1])
+    idx = np.asarray(pages[lo:hi], dtype=np.int64)
+    return kv_codes[idx]
+
+
+def gather_all(kv_codes, pages, indptr) -> np.ndarray:
+    """Every request's rows, concatenated in request order: [sum L, 576]."""
+    R = len(indptr) - 1
+    parts = [gather_rows(kv_codes, pages, indptr, r) for r in range(R)]
+    if not parts:
+        return np.zeros((0, D_QK), np.uint8)
+    return np.concatenate(parts, axis=0)
+
+
+# ---------------------------------------------------------------------------
+# Attention of one request
+# ---------------------------------------------------------------------------
+
+def attend_rows(q_rows, K, scale: float):
+    """Softmax attention of query rows over one request's dequantised rows.
+
+    ``q_rows``: float64 [n, 576] (n = qlen * H query rows of one request);
+    ``K``: float64 [L, 576] (dequantised, kv_scale applied).  Multi-query
+    form: every row attends over the same latent rows, keys are the full 576
+    dims, values the first 512 (``attend``: forward_mqa on the latent cache).
+
+    Returns ``(latent [n, 512], lse [n], p [n, L])``; for L == 0 the latent
+    is 0, the LSE -inf and p empty.
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    n = q_rows.shape[0]
+    L = K.shape[0]
+    if L == 0:
+        return np.zeros((n, D_LATENT)), np.full(n, -np.inf), np.zeros((n, 0))
+    s = scale * (q_rows @ K.T)                       # [n, L]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    denom = e.sum(axis=1, keepdims=True)
+    p = e / denom
+    lse = (m + np.log(denom))[:, 0]
+    latent = p @ K[:, :D_LATENT]
+    return latent, lse, p
+
+
+def dequant(codes, kv_scale: float) -> np.ndarray:
+    """``e4m3fn(code) * kv_scale`` in float64 (the cache holds x / k_scale as
+    fp8; ``m1c_inputs`` passes ``kv_scale=attn._k_scale_float``)."""
+    return e4m3fn_to_f64(codes) * float(kv_scale)
+
+
+def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
+           requests=None, return_p=False):
+    """The unsplit attention: latent [S, H, 512] and LSE [S, H].
+
+    ``q_bits``: uint16 bf16 bits [S, H_pad, 576]; only heads < ``heads`` are
+    read (``attend``: the real heads of a query padded 96 -> 128).
+    ``requests``: optional subset of request indices to compute (others are
+    left NaN), so that full-size workloads can be checked on a sample.
+    """
+    q = np.asarray(q_bits)
+    R = len(indptr) - 1
+    S = R * qlen
+    latent = np.full((S, heads, D_LATENT), np.nan)
+    lse = np.full((S, heads), np.nan)
+    ps = {}
+    for r in (range(R) if requests is None else requests):
+        K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
+        rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
+        lat, l, p = attend_rows(rows, K, scale)
+        latent[r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)
+        lse[r * qlen:(r + 1) * qlen] = l.reshape(qlen, heads)
+        ps[r] = p.reshape(qlen, heads, -1)
+    return (latent, lse, ps) if return_p else (latent, lse)
+
+
+# ---------------------------------------------------------------------------
+# Split-KV partials and their merge
+# ---------------------------------------------------------------------------
+
+def split_count(L: int, num_splits: int, split_tokens: int) -> int:
+    """Splits request of length L is cut into: ceil(L / split_tokens), at
+    least 1 and at most ``num_splits`` (the capacity of the partials' first
+    dimension, ``m1c_inputs``: o [splits, S, 12, 512])."""
+    if num_splits < 1 or split_tokens < 1:
+        raise ValueError("num_splits and split_tokens must be >= 1")
+    return max(1, min(num_splits, -(-int(L) // int(split_tokens))))
+
+
+def split_plan(L: int, num_splits: int, split_tokens: int):
+    """Token ranges [(start, end)] of a request's splits: n contiguous,
+    near-equal ranges, the first ``L mod n`` one token longer.  The pages do
+    not print the partition; this is the library's documented rule."""
+    n = split_count(L, num_splits, split_tokens)
+    base, rem = divmod(int(L), n)
+    out = []
+    start = 0
+    for k in range(n):
+        ln = base + (1 if k < rem else 0)
+        out.append((start, start + ln))
+        start += ln
+    assert start == L
+    return out
+
+
+def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
+                  num_splits, split_tokens, requests=None):
+    """Per-split partials: o [num_splits, S, H, 512] (float64) and lse
+    [num_splits, S, H]; each used split is the attention restricted to its
+    token range (``m1c_inputs``: new partials o [splits, S, 12, 512], LSE
+    [splits, S, 12], merged afterwards).  Unused splits hold lse = -inf and
+    o = NaN (their o is unspecified)."""
+    q = np.asarray(q_bits)
+    R = len(indptr) - 1
+    S = R * qlen
+    o = np.full((num_splits, S, heads, D_LATENT), np.nan)
+    lse = np.full((num_splits, S, heads), -np.inf)
+    if requests is not None:
+        lse[:] = np.nan
+    for r in (range(R) if requests is None else requests):
+        lse[:, r * qlen:(r + 1) * qlen] = -np.inf
+        K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
+        rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
+        for k, (a, b) in enumerate(split_plan(K.shape[0], num_splits, split_tokens)):
+            lat, l, _ = attend_rows(rows, K[a:b], scale)
+            if b > a:
+                o[k, r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)
+            lse[k, r * qlen:(r + 1) * qlen] = l.reshape(qlen, heads)
+    return o, lse
+
+
+def merge(o, lse):
+    """LSE merge of split partials into the latent (``m1c_inputs``: "M1b
+    merges the splits"; ``post``: the same LSE combine across DCP ranks).
+
+        LSE    = ln sum_k exp(lse_k)
+        latent = sum_k exp(lse_k - LSE) * o_k
+
+    Splits with lse_k = -inf are skipped, never multiplied by 0 (their o is
+    unspecified and may be NaN).  A row with every split empty gives latent
+    0 and LSE -inf.
+    """
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    K = lse.shape[0]
+    out_lse = np.full(lse.shape[1:], -np.inf)
+    latent = np.zeros(o.shape[1:])
+    valid = np.isfinite(lse)
+    any_valid = valid.any(axis=0)
+    m = np.where(valid, lse, -np.inf).max(axis=0)
+    m_safe = np.where(any_valid, m, 0.0)
+    total = np.zeros(lse.shape[1:])
+    for k in range(K):
+        w = np.where(valid[k], np.exp(np.where(valid[k], lse[k], 0.0) - m_safe), 0.0)
+        total += w
+        latent += np.where(valid[k][..., None], w[..., None] * np.nan_to_num(o[k], nan=0.0), 0.0)
+    latent = np.where(any_valid[..., None], latent / np.where(any_valid, total, 1.0)[..., None], 0.0)
+    out_lse = np.where(any_valid, m_safe + np.log(np.where(any_valid, total, 1.0)), -np.inf)
+    return latent, out_lse
+
+
+# ---------------------------------------------------------------------------
+# Absorbed value up-projection and sigmoid gate
+# ---------------------------------------------------------------------------
+
+def value_gate(latent, w_uv_bits, gate_bits, lengths, qlen):
+    """o_proj's input [S, H*128] (``post``: W_UV then the gate; ``MlaValue``
+    / ``MlaGate``: value times the sigmoid of the raw gate, rows of empty
+    requests zero).
+
+    ``latent``: float64 [S, H, 512]; ``w_uv_bits``: bf16 bits [H, 128, 512]
+    (latent axis contiguous, ``MlaValue``); ``gate_bits``: bf16 bits
+    [S, H*128]; ``lengths``: per request; row t belongs to request t // qlen.
+    Empty rows are selected to 0, never computed, so NaN gates do not leak.
+    """
+    latent = np.asarray(latent, dtype=np.float64)
+    S, H, _ = latent.shape
+    W = bf16_to_f64(w_uv_bits)                       # [H, 128, 512]
+    val = np.einsum("thc,hvc->thv", latent, W)       # [S, H, 128]
+    g = bf16_to_f64(gate_bits).reshape(S, H, D_V)
+    lens = np.asarray(lengths).astype(np.int64)
+    active = lens[np.arange(S) // qlen] > 0
+    with np.errstate(invalid="ignore"):
+        out = val * sigmoid(g)
+    out = np.where(active[:, None, None], out, 0.0)
+    return out.reshape(S, H * D_V)
+
+
+def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
+                w_uv_bits, gate_bits, lengths, requests=None):
+    """The whole step from raw inputs: (latent, lse, out).  With
+    ``requests``, only those requests' rows are filled (the rest NaN)."""
+    latent, lse = attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
+                         requests=requests)
+    lat_in = np.nan_to_num(latent, nan=0.0)
+    out = value_gate(lat_in, w_uv_bits, gate_bits, lengths, qlen)
+    if requests is not None:
+        keep = np.zeros(latent.shape[0], bool)
+        for r in requests:
+            keep[r * qlen:(r + 1) * qlen] = True
+        out[~keep] = np.nan
+    return latent, lse, out
