@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""Benchmark of one MLA decode step (attend -> merge -> value/gate) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole path over
+one batch of the workload (default: 64 single-token requests, 12 heads,
+context lengths uniform in [1024, 8192], fp8 KV), inputs resident in HBM.
+L2 is flushed (a 256 MB write) before every timed step; only the step is
+inside the CUDA events.  ``value`` is query rows (tokens) per second over
+all ranks; ``e2e`` repeats the step through the public API with the step's
+inputs copied from pinned host memory and its output read back, inside
+the timed region.  ``roofline`` is the attend kernel's algorithmic HBM bytes
+per launch over its event-timed duration, against the measured copy
+bandwidth.  ``cpu_baseline`` times the plain C fp64 oracle on the host
+cores over a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the step
+(the path has no cross-GPU exchange here); value = all ranks' rows / the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_decode_paged_gb300 as mla  # noqa: E402
+from mla_decode_paged_gb300 import workloads as W  # noqa: E402
+
+METRIC = "mla_decode_tokens_per_s"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _spec(name):
+    for s in W.WORKLOADS:
+        if s.name == name:
+            return s
+    raise SystemExit("unknown workload %s (have %s)" % (name, [s.name for s in W.WORKLOADS]))
+
+
+def _plan_stats(inp, ns, st):
+    """Host-side split counts and the attend kernel's algorithmic bytes."""
+    lens = inp.lengths.cpu().numpy().astype(np.int64)
+    n_r = np.maximum(1, np.minimum(ns, -(-lens // st)))
+    used = int(n_r[lens > 0].sum())
+    rows_per_req = inp.qlen * inp.heads
+    total = int(lens.sum())
+    R = len(lens)
+    attend_bytes = (total * (576 + 4) + (R + 1) * 4 + R * rows_per_req * 576 * 2
+                    + used * rows_per_req * (512 * 2 + 4)
+                    + int((ns - n_r).sum() + (lens == 0).sum()) * rows_per_req * 4)
+    merge_bytes = used * rows_per_req * (512 * 2 + 4) + ns * R * rows_per_req * 4 + R * rows_per_req * (1024 + 4)
+    S = R * inp.qlen
+    value_bytes = S * inp.heads * 1024 + inp.heads * 128 * 512 * 2 + 2 * S * inp.heads * 128 * 2 + R * 4
+    return dict(used_units=used, attend_bytes=attend_bytes, merge_bytes=merge_bytes, value_bytes=value_bytes,
+                kv_tokens=total, attend_flops=2 * total * rows_per_req * (576 + 512))
+
+
+class Clocks:
+    """nvidia-smi sampler running while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        busy = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_gpu(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.build()
+    spec = _spec(args.workload)
+    inp = W.make_inputs(spec, dev)
+    R, qlen, H = spec.requests, spec.qlen, spec.heads
+    S = R * qlen
+    ns, st = mla.choose_splits(R, qlen, H, inp.max_len, inp.total_len)
+    stats = _plan_stats(inp, ns, st)
+    stream = torch.cuda.current_stream(dev)
+
+    o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((ns, S, H), dtype=torch.float32, device=dev)
+    latent = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
+    lse_m = torch.empty((S, H), dtype=torch.float32, device=dev)
+    out = torch.empty((S, H * 128), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
+                   o=o, lse=lse, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    flags = mla.device_status()
+    if flags:
+        raise SystemExit("device status flags after warm-up: %#x" % flags)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    clocks.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        flush.fill_(1.0)
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    t_step = [e[0].elapsed_time(e[3]) * 1e-3 for e in evs]
+    t_att = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
+    t_mrg = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
+    t_val = [e[2].elapsed_time(e[3]) * 1e-3 for e in evs]
+    total = sum(t_step)
+
+    # ---- end to end through the public API with host buffers
+    q_h = inp.q.cpu().pin_memory()
+    gate_h = inp.gate.cpu().pin_memory()
+    pages_h = inp.pages.cpu().pin_memory()
+    indptr_h = inp.indptr.cpu().pin_memory()
+    lens_h = inp.lengths.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, gate_d = torch.empty_like(inp.q), torch.empty_like(inp.gate)
+    pages_d, indptr_d, lens_d = torch.empty_like(inp.pages), torch.empty_like(inp.indptr), torch.empty_like(inp.lengths)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h)):
+            d.copy_(h, non_blocking=True)
+        mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
+                   o=o, lse=lse, stream=stream)
+        mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
+        mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_t = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_t.append(a.elapsed_time(b) * 1e-3)
+    e2e_total = sum(e_t)
+    ok = torch.equal(out_h, out.cpu())
+
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total, e2e_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total, e2e_total = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    hbm, peak_kind = _peaks()
+    att = statistics.mean(t_att)
+    achieved = stats["attend_bytes"] / att / 1e9
+    traffic = _ncu_traffic(spec.name)
+    rec = {
+        "metric": METRIC,
+        "value": S * args.steps * ws / total,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": spec.name, "requests": R, "qlen": qlen, "heads": H, "rows": S,
+            "kv_tokens": stats["kv_tokens"], "kv_bytes": stats["kv_tokens"] * 576,
+            "num_splits": ns, "split_tokens": st, "work_units": stats["used_units"],
+            "l2": "flushed before every timed step (256 MB write, outside the events)",
+            "parallelism": "replicas" if ws > 1 else "single-gpu",
+            "kv": "fp8-e4m3 paged (page size 1)", "mma": "f16 x f16 -> f32 (attend), bf16 (W_UV)",
+        },
+        "kernels_us": {"attend": att * 1e6, "merge": statistics.mean(t_mrg) * 1e6,
+                       "value_gate": statistics.mean(t_val) * 1e6},
+        "kv_tokens_per_s": stats["kv_tokens"] * args.steps * ws / total,
+        "roofline": {
+            "kernel": "attend", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": stats["attend_bytes"], "traffic": traffic,
+        },
+        "e2e": {"value": S * args.steps * ws / e2e_total, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "output_matches_device": bool(ok)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(spec, inp)
+    return rec
+
+
+def _ncu_traffic(workload):
+    """DRAM bytes per attend launch from the committed ncu summary of the
+    current kernel, if one exists for this workload (else null)."""
+    p = os.path.join(ROOT, "profiles", "attend_%s_traffic.json" % workload)
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("current", True):
+            return d.get("dram_bytes_per_launch")
+    return None
+
+
+def cpu_baseline(spec, inp, budget_s=15.0):
+    """Time the plain C fp64 oracle on the host cores on a bounded sample of
+    the workload's requests (the first requests until ~budget_s of work)."""
+    import oracle  # test infrastructure: timed here as the CPU baseline only
+    lib = oracle.load_c()
+    threads = lib.mla_oracle_threads()
+    q = inp.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    kv = inp.kv.cpu().numpy()
+    pages = inp.pages.cpu().numpy()
+    indptr = inp.indptr.cpu().numpy()
+    w = inp.w_uv.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    g = inp.gate.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    lens = np.diff(indptr)
+    R = len(lens)
+    # estimate from a one-request probe, then take as many requests as fit the budget
+    t0 = time.perf_counter()
+    oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
+                         requests=[0])
+    probe = max(time.perf_counter() - t0, 1e-4)
+    per_token = probe / max(1, lens[0])
+    n = R
+    while n > 1 and per_token * lens[:n].sum() / max(1, min(threads, n)) > budget_s:
+        n = max(1, n // 2)
+    reqs = list(range(n))
+    t0 = time.perf_counter()
+    oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
+                         requests=reqs)
+    dt = time.perf_counter() - t0
+    return {"value": n * spec.qlen / dt, "unit": UNIT, "cores": int(threads), "kind": "oracle",
+            "sample": "%d of %d requests (%d KV tokens), full path in fp64 C, %.2f s" % (
+                n, R, int(lens[:n].sum()), dt)}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return None
+    spec = _spec(args.workload)
+    inp = W.make_inputs(spec, "cpu")
+    times = []
+    base = None
+    for k in range(args.warmup + args.steps):
+        res = cpu_baseline(spec, inp, budget_s=args.ref_budget)
+        if k >= args.warmup:
+            times.append(res)
+        base = res
+    vals = [r["value"] for r in times]
+    v = statistics.mean(vals) if vals else base["value"]
+    S = spec.requests * spec.qlen
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": S / v * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "requests": spec.requests, "qlen": spec.qlen, "heads": spec.heads,
+                   "rows": S, "note": "each step times the CPU oracle on a bounded sample of the workload"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
+                         "sample": base["sample"]},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=W.WORKLOADS[1].name)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=5.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rec = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if rec is not None:
+        print(json.dumps(rec), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA paged-decode library.
+ *
+ * One decode step of a Multi-head Latent Attention layer, in three calls:
+ *
+ *   mla_decode_attend  : bf16 absorbed queries over a paged fp8 latent KV
+ *                        cache -> split-KV partials (o, lse)
+ *   mla_merge_splits   : LSE merge of the partials -> latent
+ *   mla_value_gate     : absorbed W_UV projection fused with the sigmoid gate
+ *                        -> o_proj's input
+ *
+ * Sources (vLLM API pages):
+ *   - vllm.models.kimi_k3.amd.specialized_decode.runtime.mla: attend,
+ *     m1c_inputs, post (the decode split, the flat token rows, the padded
+ *     query, the partials and their merge);
+ *   - vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value:
+ *     MlaValue, MlaGate, value_bmm (W_UV and the gate).
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a device pointer owned by the caller, unless stated.
+ *     The library never allocates, frees or synchronises.  Each call checks
+ *     its arguments on the host, enqueues its kernel(s) on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and returns.
+ *   - Argument errors return MLA_ERR_INVALID / MLA_ERR_UNSUPPORTED before
+ *     anything is launched.  A failed launch returns MLA_ERR_CUDA;
+ *     mla_last_error() then holds the CUDA message (per host thread).
+ *   - Data errors that only the device can see (a page index outside the
+ *     pool, a non-monotone indptr, a bounded wait that ran out) never fault:
+ *     the kernel clamps the access, records a flag in a per-device status
+ *     word and carries on.  mla_device_status() reads and clears the word.
+ *   - Layouts are dense, row-major, 16-byte aligned.  Element types:
+ *     bf16 = IEEE bfloat16 bits (uint16), fp8 = OCP E4M3 ("e4m3fn") bytes.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_D_QK 576     /* query / KV row: 512 latent + 64 rope dims      */
+#define MLA_D_LATENT 512 /* latent (value) width                            */
+#define MLA_D_ROPE 64
+#define MLA_D_V 128      /* W_UV output width per head                      */
+#define MLA_MAX_HEADS 128
+#define MLA_MAX_QLEN 16
+#define MLA_MAX_SPLITS 256
+
+typedef int mla_status;
+#define MLA_OK 0
+#define MLA_ERR_INVALID (-1)     /* bad argument (null, size, stride, alignment) */
+#define MLA_ERR_UNSUPPORTED (-2) /* valid but outside what the kernels support   */
+#define MLA_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed         */
+
+/* Bits of the per-device status word (mla_device_status). */
+#define MLA_DEV_BAD_PAGE 1u      /* a page index was outside [0, pool_rows)      */
+#define MLA_DEV_BAD_INDPTR 2u    /* indptr not monotone or beyond num_pages      */
+#define MLA_DEV_TIMEOUT 4u       /* a bounded device wait ran out                */
+
+/*
+ * mla_decode_attend -- split-KV attention of one decode step.
+ *
+ * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
+ * m1c_inputs (inputs q [S, 12, 576] bf16, kv = the flat token rows, pages =
+ * paged_kv_indices, indptr = paged_kv_indptr, scale, kv_scale; outputs the
+ * partials o [splits, S, 12, 512] bf16 and LSE [splits, S, 12] f32) and
+ * attend (multi-query attention over the latent cache; a query whose row
+ * stride spans padded heads).
+ *
+ * For request r (rows t = r*qlen .. r*qlen+qlen-1), head h < heads, and
+ * the tokens j of split k's range of r:
+ *   K_j = e4m3fn(kv[pages[indptr[r] + j]]) * kv_scale        (576 wide)
+ *   s_j = scale * <q[t, h, :], K_j>
+ *   lse[k, t, h] = ln sum_j exp(s_j)
+ *   o[k, t, h, :] = sum_j exp(s_j - lse[k, t, h]) * K_j[:512]
+ * No mask within a request: every row of r attends over all of r's tokens.
+ *
+ * Split plan: request r (length L_r = indptr[r+1] - indptr[r]) is cut into
+ *   n_r = min(num_splits, max(1, ceil(L_r / split_tokens)))
+ * contiguous ranges; with b = L_r / n_r and m = L_r % n_r, split k covers
+ * [k*b + min(k, m), (k+1)*b + min(k+1, m)).  Splits k >= n_r get
+ * lse = -inf and an unspecified o.  A request with L_r = 0 has one split
+ * with lse = -inf.
+ *
+ *   q            bf16, row t head h at q + t*q_row_stride + h*576 (elements).
+ *                q_row_stride >= heads*576 and a multiple of 8; padded heads
+ *                (h >= heads) are never read.
+ *   kv           fp8 codes [pool_rows, 576], contiguous.
+ *   pages        int32 [num_pages]; indptr int32 [num_requests + 1] with
+ *                indptr[0] = 0, non-decreasing, indptr[R] <= num_pages.
+ *   qlen         query rows per request (1..16); S = num_requests * qlen.
+ *   heads        real heads (1..128).
+ *   num_splits   capacity of o / lse's first dimension (1..256).
+ *   split_tokens target tokens per split (>= 1); see mla_choose_splits.
+ *   o            bf16 [num_splits, S, heads, 512] (written);
+ *   lse          f32  [num_splits, S, heads]       (written).
+ */
+mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv,
+                             int64_t pool_rows, const int32_t *pages, int64_t num_pages,
+                             const int32_t *indptr, int num_requests, int qlen, int heads,
+                             float scale, float kv_scale, int num_splits, int split_tokens,
+                             void *o, float *lse, void *stream);
+
+/*
+ * mla_merge_splits -- LSE merge of split partials into the latent.
+ *
+ * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
+ * m1c_inputs ("M1b merges the splits") and post (the same LSE combine
+ * across decode-context-parallel ranks).  For every row t < rows, head h:
+ *   LSE = ln sum_k exp(lse[k, t, h])   over splits with lse > -inf
+ *   latent[t, h, :] = sum_k exp(lse[k, t, h] - LSE) * o[k, t, h, :]
+ * Splits with lse = -inf are skipped (their o is never read).  A row whose
+ * splits are all empty gets latent 0 and LSE -inf.
+ *
+ *   o        bf16 [num_splits, rows, heads, 512]; lse f32 [num_splits, rows, heads]
+ *   latent   bf16 [rows, heads, 512] (written)
+ *   lse_out  f32  [rows, heads] (written; may be NULL)
+ */
+mla_status mla_merge_splits(const void *o, const float *lse, int num_splits, int rows,
+                            int heads, void *latent, float *lse_out, void *stream);
+
+/*
+ * mla_value_gate -- absorbed W_UV projection fused with the sigmoid gate.
+ *
+ * Defined by: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value,
+ * MlaValue (W_UV on the [B, H, 512] bf16 latent with bf16 MMA and fp32
+ * accumulation; W_UV with a contiguous latent axis; rows are tokens, qlen
+ * per request) and MlaGate (the bf16 value times the fp32 sigmoid of the
+ * gate, rounded to bf16; rows of empty requests zero).  For row t, head h,
+ * output v < 128, with r = t / qlen:
+ *   val = bf16( sum_c latent[t, h, c] * w_uv[h, v, c] )      (fp32 sum)
+ *   out[t, h*128 + v] = lengths[r] > 0 ? bf16( f32(val) * sigmoid(f32(gate[t, h*128 + v])) ) : 0
+ * The zeroing is a select, so NaN gates of empty rows never reach out.
+ *
+ *   latent   bf16 [S, heads, 512];  w_uv bf16 [heads, 128, 512]
+ *   gate     bf16 [S, heads*128] (raw logits);  lengths int32 [num_requests]
+ *   out      bf16 [S, heads*128] (written);  S = num_requests * qlen
+ */
+mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate,
+                          const int32_t *lengths, int num_requests, int qlen, int heads,
+                          void *out, void *stream);
+
+/*
+ * mla_choose_splits -- a split plan for mla_decode_attend from host-known
+ * sizes (no device read).  Returns num_splits (>= 1) and writes
+ * *split_tokens so that the longest request (max_len) is cut into
+ * num_splits ranges and the total work spreads over ~sm_count SMs.
+ * sm_count <= 0 means the current device's SM count.
+ */
+int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
+                      int sm_count, int *split_tokens);
+
+/*
+ * mla_debug_gather -- copies every request's KV rows, in request order, to
+ * out (fp8 codes [indptr[R], 576]) through the attend kernel's own row
+ * addressing and bulk-copy code, so that page indexing can be checked
+ * byte for byte.  Same pointer rules as mla_decode_attend.
+ */
+mla_status mla_debug_gather(const void *kv, int64_t pool_rows, const int32_t *pages,
+                            int64_t num_pages, const int32_t *indptr, int num_requests,
+                            int64_t total_rows, void *out, void *stream);
+
+/*
+ * mla_device_status -- synchronises `stream`, returns the current device's
+ * status word (MLA_DEV_* bits set by kernels since the last read) in
+ * *flags and clears it.  Returns MLA_ERR_CUDA if the synchronisation fails.
+ */
+mla_status mla_device_status(void *stream, unsigned int *flags);
+
+/* Static description of a status code. */
+const char *mla_status_string(mla_status status);
+
+/* Detail of the last error on this host thread ("" if none). */
+const char *mla_last_error(void);
+
+/* Library version string. */
+const char *mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

@@ -1,1 +1,225 @@
-"""GB300-native MLA paged decode (placeholder; binding added with the library)."""
+"""GB300-native (sm_103a) MLA paged decode: a thin Python binding over the
+C ABI in ``include/mla_decode.h``.
+
+The three calls of one decode step of a Multi-head Latent Attention layer:
+
+    o, lse = attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens)
+    latent, lse_merged = merge(o, lse)
+    out = value_gate(latent, w_uv, gate, lengths, qlen)
+
+This module only marshals arguments: it checks dtypes / shapes, allocates
+outputs with torch (device memory), passes raw pointers and the current CUDA
+stream to the native library, and turns error codes into exceptions.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback.  If the library has not been built (``build()``), every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+D_QK, D_LATENT, D_V = 576, 512, 128
+MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
+DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
+
+__all__ = ["attend", "merge", "value_gate", "decode_step", "choose_splits", "debug_gather",
+           "device_status", "build", "library", "MlaError"]
+
+
+class MlaError(RuntimeError):
+    """A non-zero status from the native library."""
+
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__("%s failed: %s (%d)%s" % (where, _status_name(status), status,
+                                                  ": " + detail if detail else ""))
+        self.status = status
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library in-tree (sm_103a) and return its path."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def library() -> ctypes.CDLL:
+    """The loaded native library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError("mla_decode_paged_gb300: native library %s is missing; run "
+                           "mla_decode_paged_gb300.build() first (no CPU fallback exists)" % path)
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.mla_decode_attend.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32,
+                                      vp, vp, vp]
+    lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
+    lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
+    lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    for name in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate", "mla_debug_gather",
+                 "mla_device_status", "mla_choose_splits"):
+        getattr(lib, name).restype = ctypes.c_int
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_last_error.restype = ctypes.c_char_p
+    lib.mla_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return library().mla_status_string(status).decode()
+    except Exception:  # pragma: no cover - only when the library is absent
+        return "status"
+
+
+def _check(status: int, where: str):
+    if status != MLA_OK:
+        raise MlaError(status, where, library().mla_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _as_u8(kv: torch.Tensor) -> torch.Tensor:
+    if kv.dtype == torch.float8_e4m3fn:
+        kv = kv.view(torch.uint8)
+    _need(kv.dtype == torch.uint8, "kv must be uint8 codes or float8_e4m3fn")
+    return kv
+
+
+def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
+           o=None, lse=None, stream=None):
+    """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
+    lse [num_splits, S, heads] f32)``.
+
+    ``q``: bf16 ``[S, H_pad, 576]`` whose rows may be strided (a padded query:
+    ``heads`` < H_pad reads only the first ``heads``); ``kv``: ``[pool, 576]``
+    fp8 codes; ``pages``/``indptr``: int32; S = (len(indptr) - 1) * qlen.
+    """
+    kv = _as_u8(kv)
+    heads = q.shape[1] if heads is None else heads
+    R = indptr.numel() - 1
+    S = R * qlen
+    _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == D_QK, "q must be bf16 [S, H, 576]")
+    _need(q.stride(2) == 1 and q.stride(1) == D_QK, "q rows must have contiguous [H, 576] heads")
+    _need(q.shape[0] == S and heads <= q.shape[1], "q shape does not match indptr / qlen / heads")
+    _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
+    _need(pages.dtype == torch.int32 and indptr.dtype == torch.int32, "pages / indptr must be int32")
+    _need(pages.is_contiguous() and indptr.is_contiguous(), "pages / indptr must be contiguous")
+    if o is None:
+        o = torch.empty((num_splits, S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((num_splits, S, heads), dtype=torch.float32, device=q.device)
+    st = library().mla_decode_attend(
+        _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr), R, qlen,
+        heads, float(scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o), _ptr(lse),
+        ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_decode_attend")
+    return o, lse
+
+
+def merge(o, lse, *, latent=None, lse_out=None, want_lse=True, stream=None):
+    """LSE merge: returns ``(latent [S, heads, 512] bf16, lse [S, heads] f32 or None)``."""
+    _need(o.dtype == torch.bfloat16 and o.dim() == 4 and o.shape[3] == D_LATENT and o.is_contiguous(),
+          "o must be contiguous bf16 [splits, S, heads, 512]")
+    _need(lse.dtype == torch.float32 and lse.shape == o.shape[:3] and lse.is_contiguous(),
+          "lse must be contiguous f32 [splits, S, heads]")
+    ns, S, H = o.shape[:3]
+    if latent is None:
+        latent = torch.empty((S, H, D_LATENT), dtype=torch.bfloat16, device=o.device)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((S, H), dtype=torch.float32, device=o.device)
+    st = library().mla_merge_splits(_ptr(o), _ptr(lse), ns, S, H, _ptr(latent), _ptr(lse_out),
+                                    ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_merge_splits")
+    return latent, lse_out
+
+
+def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
+    """W_UV + sigmoid gate: returns ``out [S, heads*128] bf16``."""
+    _need(latent.dtype == torch.bfloat16 and latent.dim() == 3 and latent.shape[2] == D_LATENT
+          and latent.is_contiguous(), "latent must be contiguous bf16 [S, heads, 512]")
+    S, H = latent.shape[:2]
+    _need(w_uv.dtype == torch.bfloat16 and tuple(w_uv.shape) == (H, D_V, D_LATENT) and w_uv.is_contiguous(),
+          "w_uv must be contiguous bf16 [heads, 128, 512]")
+    _need(gate.dtype == torch.bfloat16 and tuple(gate.shape) == (S, H * D_V) and gate.is_contiguous(),
+          "gate must be contiguous bf16 [S, heads*128]")
+    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S, "lengths must be int32 [S / qlen]")
+    if out is None:
+        out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=latent.device)
+    st = library().mla_value_gate(_ptr(latent), _ptr(w_uv), _ptr(gate), _ptr(lengths), lengths.numel(), qlen,
+                                  H, _ptr(out), ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_value_gate")
+    return out
+
+
+def choose_splits(num_requests, qlen, heads, max_len, total_len=0, sm_count=0):
+    """Host-side split plan: returns ``(num_splits, split_tokens)``."""
+    st = ctypes.c_int(0)
+    ns = library().mla_choose_splits(int(num_requests), int(qlen), int(heads), int(max_len), int(total_len),
+                                     int(sm_count), ctypes.byref(st))
+    return int(ns), int(st.value)
+
+
+def debug_gather(kv, pages, indptr, total_rows=None, stream=None):
+    """Every request's KV rows in request order ([sum L, 576] uint8), gathered
+    by the attend kernels' own row addressing."""
+    kv = _as_u8(kv)
+    if total_rows is None:
+        total_rows = int(indptr[-1].item())
+    out = torch.empty((total_rows, D_QK), dtype=torch.uint8, device=kv.device)
+    st = library().mla_debug_gather(_ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
+                                    indptr.numel() - 1, total_rows, _ptr(out), ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_debug_gather")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream, return and clear the device status bits
+    (DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT)."""
+    flags = ctypes.c_uint(0)
+    _check(library().mla_device_status(ctypes.c_void_p(_stream(stream)), ctypes.byref(flags)),
+           "mla_device_status")
+    return int(flags.value)
+
+
+def decode_step(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, *, heads=None, qlen=1,
+                num_splits=None, split_tokens=None, max_len=None, total_len=0, stream=None):
+    """The whole step (attend -> merge -> value_gate); returns
+    ``(out, latent, lse)``.  Without a split plan one is chosen from
+    ``max_len`` (host-known longest request)."""
+    heads = q.shape[1] if heads is None else heads
+    if num_splits is None or split_tokens is None:
+        if max_len is None:
+            raise ValueError("give num_splits and split_tokens, or max_len for the split plan")
+        num_splits, split_tokens = choose_splits(indptr.numel() - 1, qlen, heads, max_len, total_len)
+    o, lse = attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, heads=heads,
+                    qlen=qlen, stream=stream)
+    latent, lse_m = merge(o, lse, stream=stream)
+    out = value_gate(latent, w_uv, gate, lengths, qlen, stream=stream)
+    return out, latent, lse_m

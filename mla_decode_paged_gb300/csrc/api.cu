@@ -1,0 +1,202 @@
+// Host side of the C ABI declared in include/mla_decode.h: argument
+// validation (before any launch), kernel dispatch, the split-plan
+// heuristic, error strings and the device status word.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+cudaError_t attend_mma_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R,
+                              int qlen, int heads, float scale, float kv_scale, int num_splits,
+                              int split_tokens, void *o, float *lse, int grid, cudaStream_t st);
+cudaError_t attend_mma_status(unsigned int *flags, bool clear);
+cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
+                         void *latent, float *lse_out, cudaStream_t st);
+cudaError_t merge_status(unsigned int *flags, bool clear);
+cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *gate,
+                              const int32_t *lengths, int R, int qlen, int H, void *out, cudaStream_t st);
+cudaError_t value_gate_status(unsigned int *flags, bool clear);
+cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
+                          int R, int64_t total_rows, void *out, cudaStream_t st);
+cudaError_t gather_status(unsigned int *flags, bool clear);
+}  // namespace mla
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mla_status fail(mla_status s, const char *msg) {
+    g_last_error = msg;
+    return s;
+}
+
+mla_status cuda_fail(cudaError_t e, const char *where) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+    return MLA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                             const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                             int num_requests, int qlen, int heads, float scale, float kv_scale,
+                             int num_splits, int split_tokens, void *o, float *lse, void *stream) {
+    if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
+    if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
+    if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
+    if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return fail(MLA_ERR_INVALID, "num_splits outside 1..256");
+    if (split_tokens < 1) return fail(MLA_ERR_INVALID, "split_tokens < 1");
+    if (q_row_stride < (int64_t)heads * MLA_D_QK || q_row_stride % 8 != 0)
+        return fail(MLA_ERR_INVALID, "q_row_stride must be >= heads*576 and a multiple of 8");
+    if (pool_rows < 0 || num_pages < 0) return fail(MLA_ERR_INVALID, "negative pool_rows / num_pages");
+    if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return fail(MLA_ERR_INVALID, "non-finite scale");
+    if (num_requests == 0) return MLA_OK;
+    if (!q || !kv || !indptr || !o || !lse || (num_pages > 0 && !pages))
+        return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(indptr, 4) || !aligned(pages, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (q, kv, o need 16 bytes)");
+    if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
+                                           num_requests, qlen, heads, scale, kv_scale, num_splits,
+                                           split_tokens, o, lse, device_sms(), st);
+    if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+    return MLA_OK;
+}
+
+mla_status mla_merge_splits(const void *o, const float *lse, int num_splits, int rows, int heads,
+                            void *latent, float *lse_out, void *stream) {
+    if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return fail(MLA_ERR_INVALID, "num_splits outside 1..256");
+    if (rows < 0) return fail(MLA_ERR_INVALID, "rows < 0");
+    if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
+    if (rows == 0) return MLA_OK;
+    if (!o || !lse || !latent) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(o, 16) || !aligned(latent, 16) || !aligned(lse, 4) || !aligned(lse_out, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (o, latent need 16 bytes)");
+    cudaError_t e = mla::merge_launch(o, lse, num_splits, rows, heads, latent, lse_out,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return MLA_OK;
+}
+
+mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate, const int32_t *lengths,
+                          int num_requests, int qlen, int heads, void *out, void *stream) {
+    if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
+    if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
+    if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
+    if (num_requests == 0) return MLA_OK;
+    if (!latent || !w_uv || !gate || !lengths || !out) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(latent, 16) || !aligned(w_uv, 16) || !aligned(gate, 4) || !aligned(out, 4) ||
+        !aligned(lengths, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (latent, w_uv need 16 bytes)");
+    if ((int64_t)num_requests * qlen > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
+    cudaError_t e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "value_gate launch");
+    return MLA_OK;
+}
+
+int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len, int sm_count,
+                      int *split_tokens) {
+    // Cost model: units are dealt round-robin to one persistent CTA per SM,
+    // so the busiest CTA runs ceil(units * groups / SMs) units of ~st
+    // tokens, each with a fixed start-up cost; the partials cost a write in
+    // attend and a read in the merge.  Pick the split count with the
+    // smallest modelled time.
+    if (sm_count <= 0) sm_count = device_sms();
+    if (num_requests <= 0 || max_len <= 0) {
+        if (split_tokens) *split_tokens = 1 << 20;
+        return 1;
+    }
+    if (total_len <= 0) total_len = (int64_t)num_requests * max_len;
+    const int rows = qlen * heads;
+    const int groups = (rows + 63) / 64;
+    const double bw_sm = 6.5e12 / sm_count;         // bytes/s per SM at the HBM roofline
+    const double t_unit = 1.5e-6;                     // per-unit start-up (query load, epilogue)
+    const double avg_fill = (double)total_len / ((double)num_requests * max_len);
+    int best_ns = 1, best_st = max_len;
+    double best_t = 1e30;
+    for (int ns = 1; ns <= MLA_MAX_SPLITS; ++ns) {
+        const int st = (max_len + ns - 1) / ns;
+        if (st < 64 && ns > 1) break;
+        const double units = std::ceil((double)total_len / st + 0.5 * num_requests * (1.0 - avg_fill));
+        const double per_cta = std::ceil(units * groups / sm_count);
+        const double t_kv = per_cta * (st * (double)MLA_D_QK / bw_sm + t_unit);
+        const double t_part = units * rows * (MLA_D_LATENT * 2.0 + 4.0) * 2.0 / (bw_sm * sm_count);
+        const double t = t_kv + t_part;
+        if (t < best_t * 0.999) {
+            best_t = t;
+            best_ns = ns;
+            best_st = st;
+        }
+    }
+    if (split_tokens) *split_tokens = best_st;
+    return best_ns;
+}
+
+mla_status mla_debug_gather(const void *kv, int64_t pool_rows, const int32_t *pages, int64_t num_pages,
+                            const int32_t *indptr, int num_requests, int64_t total_rows, void *out,
+                            void *stream) {
+    if (num_requests < 0 || total_rows < 0 || pool_rows < 0 || num_pages < 0)
+        return fail(MLA_ERR_INVALID, "negative size");
+    if (total_rows > num_pages) return fail(MLA_ERR_INVALID, "total_rows > num_pages");
+    if (total_rows == 0) return MLA_OK;
+    if (!kv || !pages || !indptr || !out) return fail(MLA_ERR_INVALID, "null pointer");
+    if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    if (!aligned(kv, 16) || !aligned(out, 16) || !aligned(pages, 4) || !aligned(indptr, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (kv, out need 16 bytes)");
+    cudaError_t e = mla::gather_launch(kv, pool_rows, pages, indptr, num_requests, total_rows, out,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    return MLA_OK;
+}
+
+mla_status mla_device_status(void *stream, unsigned int *flags) {
+    if (!flags) return fail(MLA_ERR_INVALID, "null flags");
+    *flags = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::merge_status,
+                                                      mla::value_gate_status, mla::gather_status};
+    for (auto rd : readers) {
+        unsigned int f = 0;
+        e = rd(&f, true);
+        if (e != cudaSuccess) return cuda_fail(e, "status read");
+        *flags |= f;
+    }
+    return MLA_OK;
+}
+
+const char *mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported argument";
+        case MLA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+const char *mla_last_error(void) { return g_last_error.c_str(); }
+
+const char *mla_version(void) { return "mla_decode_paged_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+the header declares, rejects bad arguments on the host before any launch,
+and its split-plan helper is sane.  No kernel runs here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_decode_paged_gb300 as mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla.build()
+    return mla.library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_three_calls():
+    names = _declared()
+    for n in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.mla_version()
+    assert lib.mla_status_string(0) == b"ok"
+    assert lib.mla_status_string(-1) == b"invalid argument"
+
+
+NULL = ctypes.c_void_p(0)
+P16 = ctypes.c_void_p(1 << 20)  # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(qlen=0), b"qlen"),
+    (dict(qlen=17), b"qlen"),
+    (dict(heads=0), b"heads"),
+    (dict(heads=129), b"heads"),
+    (dict(num_splits=0), b"num_splits"),
+    (dict(num_splits=257), b"num_splits"),
+    (dict(split_tokens=0), b"split_tokens"),
+    (dict(q_row_stride=12 * 576 - 8), b"q_row_stride"),
+    (dict(q_row_stride=12 * 576 + 4), b"q_row_stride"),
+    (dict(q=NULL), b"null"),
+    (dict(o=NULL), b"null"),
+    (dict(q=ctypes.c_void_p((1 << 20) + 8)), b"misaligned"),
+    (dict(pool_rows=0), b"empty KV pool"),
+    (dict(scale=float("nan")), b"non-finite"),
+])
+def test_attend_rejects_bad_arguments(lib, kw, msg):
+    a = dict(q=P16, q_row_stride=12 * 576, kv=P16, pool_rows=100, pages=P16, num_pages=10, indptr=P16,
+             R=2, qlen=1, heads=12, scale=0.1, kv_scale=1.0, num_splits=4, split_tokens=16, o=P16, lse=P16,
+             stream=NULL)
+    a.update(kw)
+    f = lib.mla_decode_attend
+    st = f(a["q"], a["q_row_stride"], a["kv"], a["pool_rows"], a["pages"], a["num_pages"], a["indptr"],
+           a["R"], a["qlen"], a["heads"], a["scale"], a["kv_scale"], a["num_splits"], a["split_tokens"],
+           a["o"], a["lse"], a["stream"])
+    assert st == mla.MLA_ERR_INVALID
+    assert msg in lib.mla_last_error()
+
+
+def test_merge_and_value_gate_reject_bad_arguments(lib):
+    assert lib.mla_merge_splits(P16, P16, 0, 4, 12, P16, NULL, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_merge_splits(P16, P16, 2, 4, 0, P16, NULL, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_merge_splits(NULL, P16, 2, 4, 12, P16, NULL, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_value_gate(P16, P16, P16, P16, 2, 0, 12, P16, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_value_gate(P16, NULL, P16, P16, 2, 1, 12, P16, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_debug_gather(P16, 10, P16, 5, P16, 1, 6, P16, NULL) == mla.MLA_ERR_INVALID
+    # empty work is a no-op, not an error (and launches nothing)
+    assert lib.mla_merge_splits(P16, P16, 2, 0, 12, P16, NULL, NULL) == mla.MLA_OK
+    assert lib.mla_value_gate(P16, P16, P16, P16, 0, 1, 12, P16, NULL) == mla.MLA_OK
+
+
+@pytest.mark.parametrize("R,qlen,H,max_len,total", [
+    (2, 1, 12, 100, 164), (64, 1, 12, 8192, 295000), (128, 4, 12, 32768, 2359000),
+    (32, 1, 96, 32768, 1 << 20), (256, 8, 12, 131072, 4700000), (1, 1, 12, 1, 1), (8, 16, 128, 500, 2000)])
+def test_choose_splits_plan_is_valid(R, qlen, H, max_len, total):
+    ns, st = mla.choose_splits(R, qlen, H, max_len, total, sm_count=152)
+    assert 1 <= ns <= 256 and st >= 1
+    assert -(-max_len // st) <= ns          # the longest request fits in ns splits of st tokens
+    if max_len * R >= 1 << 20:
+        assert ns >= 2                      # long work is split to fill the SMs

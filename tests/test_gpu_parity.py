@@ -1,0 +1,243 @@
+"""GPU parity of the CUDA path against the fp64 CPU oracle, element by
+element, through the C ABI (via the thin binding).
+
+Small cases span several 128-token tiles and a ragged tail and run the
+oracle on everything; the five full-size workloads run in the launch
+configuration the benchmark times (split plan from mla_choose_splits) and
+are checked on sampled requests the oracle computes one by one."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_decode_paged_gb300 as mla
+from mla_decode_paged_gb300 import workloads as W
+from oracle import mla_oracle as O
+from tests._bits import bf16_bits, i32, oracle_args, u8
+from tests.parity import assert_bf16_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mla.build()
+    mla.device_status()  # clear any stale bits
+    yield
+
+
+def _to(inp, device):
+    out = W.Inputs(inp.spec, *(getattr(inp, f).to(device) for f in
+                               ("q", "kv", "pages", "indptr", "lengths", "w_uv", "gate")),
+                   inp.scale, inp.kv_scale)
+    return out
+
+
+def _run_path(inp, ns, st):
+    o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st,
+                        heads=inp.heads, qlen=inp.qlen)
+    latent, lse_m = mla.merge(o, lse)
+    out = mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, inp.qlen)
+    torch.cuda.synchronize()
+    return o, lse, latent, lse_m, out
+
+
+def _check_partials(o, lse, inp_cpu, ns, st):
+    ro, rl = O.attend_splits(**oracle_args(inp_cpu), num_splits=ns, split_tokens=st)
+    assert_lse_close(lse, rl, "partial lse")
+    used = np.isfinite(rl)                      # o of empty / unused splits is unspecified
+    assert_bf16_close(o, ro, "partial o", mask=used)
+
+
+def _check_full(latent, lse_m, out, inp_cpu):
+    a = oracle_args(inp_cpu)
+    rlat, rlse, rout = O.decode_step(**a, w_uv_bits=bf16_bits(inp_cpu.w_uv),
+                                     gate_bits=bf16_bits(inp_cpu.gate), lengths=i32(inp_cpu.lengths))
+    assert_lse_close(lse_m, rlse, "merged lse")
+    assert_bf16_close(latent, rlat, "latent")
+    assert_bf16_close(out, rout, "out")
+    empty = np.repeat(i32(inp_cpu.lengths) == 0, inp_cpu.qlen)
+    if empty.any():
+        assert torch.all(out[torch.from_numpy(empty).to(out.device)] == 0)
+
+
+# ------------------------------------------------------------------ small cases
+
+SMALL = [
+    # (workload index, lengths)  -- spans several tiles, ragged tails, empty requests
+    (0, None),
+    (1, [1, 17, 128, 129, 300, 1000]),
+    (2, [257, 64, 700]),
+    (3, [300, 129]),
+    (4, [0, 5, 200, 0, 333]),
+]
+
+
+@pytest.mark.parametrize("idx,lengths", SMALL)
+@pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (8, 50), (3, 7), "auto"])
+def test_small_workloads_match_oracle(idx, lengths, plan):
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    if plan == "auto":
+        plan = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, inp.max_len, inp.total_len)
+    ns, st = plan
+    o, lse, latent, lse_m, out = _run_path(inp, ns, st)
+    _check_partials(o, lse, inp_cpu, ns, st)
+    _check_full(latent, lse_m, out, inp_cpu)
+    assert mla.device_status() == 0
+
+
+@pytest.mark.parametrize("heads,qlen", [(16, 1), (12, 2), (7, 5), (16, 4), (128, 1), (20, 5), (1, 1), (128, 16)])
+def test_row_counts_and_groups(heads, qlen):
+    """Query-row counts that select each row-tile size and several row groups."""
+    spec = W.WorkloadSpec("rows", 11, 3, qlen, heads, heads + (8 if heads < 128 else 0),
+                          "fixed:150,40,1", 0.7)
+    lengths = [150, 40, 1] if heads * qlen <= 512 else [40, 3, 1]
+    inp_cpu = W.make_inputs(spec, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 2, 64)
+    _check_partials(o, lse, inp_cpu, 2, 64)
+    _check_full(latent, lse_m, out, inp_cpu)
+
+
+def test_peaky_scores():
+    """A large softmax scale makes attention peaky, so outputs are O(0.1-1)
+    and the element-wise bound is tight."""
+    inp_cpu = W.make_inputs(0, "cpu")
+    inp_cpu.scale = 1.0
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 4, 25)
+    lat_ref, _ = O.attend(**oracle_args(inp_cpu))
+    assert np.abs(lat_ref).max() > 0.1
+    _check_partials(o, lse, inp_cpu, 4, 25)
+    _check_full(latent, lse_m, out, inp_cpu)
+
+
+def test_all_requests_empty():
+    inp_cpu = W.make_inputs(4, "cpu", lengths=[0, 0, 0])
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 4, 16)
+    assert torch.all(torch.isneginf(lse)) and torch.all(torch.isneginf(lse_m))
+    assert torch.all(latent == 0) and torch.all(out == 0)
+
+
+def test_unused_splits_have_neg_inf_lse():
+    inp_cpu = W.make_inputs(1, "cpu", lengths=[10, 300])
+    inp = _to(inp_cpu, DEV)
+    o, lse, *_ = _run_path(inp, 16, 64)
+    # request 0: 1 split; request 1: ceil(300/64) = 5 splits
+    assert torch.all(torch.isneginf(lse[1:, 0])) and torch.isfinite(lse[0, 0]).all()
+    assert torch.isfinite(lse[:5, 1]).all() and torch.all(torch.isneginf(lse[5:, 1]))
+
+
+def test_padded_heads_never_read():
+    inp_cpu = W.make_inputs(3, "cpu", lengths=[70, 33])
+    assert torch.isnan(inp_cpu.q[:, 96:].float()).all()
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 2, 40)
+    assert torch.isfinite(latent).all() and torch.isfinite(out).all()
+    _check_full(latent, lse_m, out, inp_cpu)
+
+
+# --------------------------------------------------------------- merge / value
+
+@pytest.mark.parametrize("splits,rows,heads", [(1, 3, 12), (5, 17, 12), (40, 9, 7), (256, 2, 3)])
+def test_merge_standalone(splits, rows, heads):
+    o, lse = W.make_partials(splits, rows, heads, seed=splits)
+    lat, ls = mla.merge(o.to(DEV), lse.to(DEV))
+    rl, rs = O.merge(O.bf16_to_f64(bf16_bits(o)), lse.double().numpy())
+    assert_lse_close(ls, rs, "merge lse")
+    assert_bf16_close(lat, rl, "merge latent")
+
+
+@pytest.mark.parametrize("R,qlen,heads", [(3, 1, 12), (70, 1, 12), (5, 4, 12), (9, 8, 12), (2, 1, 96), (1, 3, 5)])
+def test_value_gate_standalone(R, qlen, heads):
+    S = R * qlen
+    lat = W.make_latent(S, heads, seed=R)
+    g = torch.Generator().manual_seed(R)
+    w = (torch.randn(heads, 128, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    gate = torch.randn(S, heads * 128, generator=g).to(torch.bfloat16)
+    lengths = torch.randint(0, 3, (R,), generator=g, dtype=torch.int32)
+    for r in range(R):
+        if lengths[r] == 0:
+            gate[r * qlen:(r + 1) * qlen] = float("nan")
+    out = mla.value_gate(lat.to(DEV), w.to(DEV), gate.to(DEV), lengths.to(DEV), qlen)
+    ref = O.value_gate(O.bf16_to_f64(bf16_bits(lat)), bf16_bits(w), bf16_bits(gate), lengths.numpy(), qlen)
+    assert_bf16_close(out, ref, "value_gate")
+    dead = np.repeat(lengths.numpy() == 0, qlen)
+    assert torch.all(out[torch.from_numpy(dead).to(DEV)] == 0)
+
+
+# ----------------------------------------------------------------- page gather
+
+@pytest.mark.parametrize("idx,lengths", SMALL)
+def test_gather_bit_exact_small(idx, lengths):
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    rows = mla.debug_gather(inp.kv, inp.pages, inp.indptr)
+    ref = O.gather_all(u8(inp_cpu.kv), i32(inp_cpu.pages), i32(inp_cpu.indptr))
+    assert np.array_equal(u8(rows), ref)
+
+
+def test_gather_bit_exact_full_decode_batch():
+    inp = W.make_inputs(1, DEV)
+    rows = mla.debug_gather(inp.kv, inp.pages, inp.indptr)
+    ref = O.gather_all(u8(inp.kv), i32(inp.pages), i32(inp.indptr))
+    assert np.array_equal(u8(rows), ref)
+
+
+def test_bad_pages_and_indptr_are_flagged_not_faulted():
+    inp_cpu = W.make_inputs(0, "cpu")
+    inp = _to(inp_cpu, DEV)
+    bad = inp.pages.clone()
+    bad[3] = inp.kv.shape[0] + 5          # outside the pool: clamped + flagged
+    bad[7] = -2
+    mla.attend(inp.q, inp.kv, bad, inp.indptr, inp.scale, inp.kv_scale, 1, 1 << 20)
+    assert mla.device_status() & mla.DEV_BAD_PAGE
+    bad_ip = inp.indptr.clone()
+    bad_ip[1] = bad_ip[2] + 1             # decreasing: request treated as empty + flagged
+    mla.attend(inp.q, inp.kv, inp.pages, bad_ip, inp.scale, inp.kv_scale, 1, 1 << 20)
+    assert mla.device_status() & mla.DEV_BAD_INDPTR
+    assert mla.device_status() == 0
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def _sample_requests(lengths, k=2, seed=0):
+    lens = np.asarray(lengths)
+    pick = {int(lens.argmax()), int(np.where(lens > 0, lens, lens.max() + 1).argmin())}
+    zero = np.where(lens == 0)[0]
+    if zero.size:
+        pick.add(int(zero[0]))
+    rng = np.random.default_rng(seed)
+    pick |= set(int(x) for x in rng.choice(len(lens), size=min(k, len(lens)), replace=False))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size_workloads_sampled(idx):
+    inp = W.make_inputs(idx, DEV)
+    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, inp.max_len, inp.total_len)
+    _, _, latent, lse_m, out = _run_path(inp, ns, st)
+    lens = i32(inp.lengths)
+    reqs = _sample_requests(lens, seed=idx)
+    a = dict(q_bits=bf16_bits(inp.q), kv_codes=u8(inp.kv), pages=i32(inp.pages), indptr=i32(inp.indptr),
+             scale=inp.scale, kv_scale=inp.kv_scale, heads=inp.heads, qlen=inp.qlen)
+    rlat, rlse, rout = O.decode_step(**a, w_uv_bits=bf16_bits(inp.w_uv), gate_bits=bf16_bits(inp.gate),
+                                     lengths=lens, requests=reqs)
+    rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
+    assert_lse_close(lse_m[rows], rlse[rows], "lse (sampled)")
+    assert_bf16_close(latent[rows], rlat[rows], "latent (sampled)")
+    assert_bf16_close(out[rows], rout[rows], "out (sampled)")
+    # properties that hold at any size, on every row
+    assert torch.isfinite(latent).all() and torch.isfinite(out).all()
+    dead = torch.from_numpy(np.repeat(lens == 0, inp.qlen)).to(DEV)
+    assert torch.all(out[dead] == 0) and torch.all(torch.isneginf(lse_m[dead]))
+    assert torch.isfinite(lse_m[~dead]).all()
+    assert mla.device_status() == 0
