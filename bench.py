@@ -148,7 +148,7 @@ def run_gpu(args):
     inp = W.make_inputs(spec, dev)
     R, qlen, H = spec.requests, spec.qlen, spec.heads
     S = R * qlen
-    ns, st = mla.choose_splits(R, qlen, H, inp.max_len, inp.total_len)
+    ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
     stats = _plan_stats(inp, ns, st)
     stream = torch.cuda.current_stream(dev)
 

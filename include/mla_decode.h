@@ -145,12 +145,16 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
 /*
  * mla_choose_splits -- a split plan for mla_decode_attend from host-known
  * sizes (no device read).  Returns num_splits (>= 1) and writes
- * *split_tokens so that the longest request (max_len) is cut into
- * num_splits ranges and the total work spreads over ~sm_count SMs.
+ * *split_tokens.  The plan minimises a model of the attend time: work units
+ * are dealt round-robin to one persistent CTA per SM, so the busiest CTA
+ * sets the time; every unit costs a fixed start-up plus its KV bytes, and
+ * the partials cost a write and a read.  With host_lengths (int32 [R], host
+ * memory, may be NULL) the unit sizes are exact; otherwise they are
+ * estimated from max_len and total_len (total_len <= 0: R * max_len).
  * sm_count <= 0 means the current device's SM count.
  */
 int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
-                      int sm_count, int *split_tokens);
+                      const int32_t *host_lengths, int sm_count, int *split_tokens);
 
 /*
  * mla_debug_gather -- copies every request's KV rows, in request order, to

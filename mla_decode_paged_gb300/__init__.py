@@ -64,7 +64,7 @@ def library() -> ctypes.CDLL:
                                       vp, vp, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
-    lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     for name in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate", "mla_debug_gather",
@@ -178,10 +178,18 @@ def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
     return out
 
 
-def choose_splits(num_requests, qlen, heads, max_len, total_len=0, sm_count=0):
-    """Host-side split plan: returns ``(num_splits, split_tokens)``."""
+def choose_splits(num_requests, qlen, heads, max_len=0, total_len=0, sm_count=0, lengths=None):
+    """Host-side split plan: returns ``(num_splits, split_tokens)``.
+    ``lengths`` (host-known per-request lengths, any int sequence or CPU
+    tensor) makes the plan exact; otherwise ``max_len`` / ``total_len``
+    estimate it."""
     st = ctypes.c_int(0)
+    host = None
+    if lengths is not None:
+        host = torch.as_tensor(lengths, dtype=torch.int32, device="cpu").contiguous()
+        num_requests = host.numel()
     ns = library().mla_choose_splits(int(num_requests), int(qlen), int(heads), int(max_len), int(total_len),
+                                     None if host is None else ctypes.c_void_p(host.data_ptr()),
                                      int(sm_count), ctypes.byref(st))
     return int(ns), int(st.value)
 

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -114,34 +115,59 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
     return MLA_OK;
 }
 
-int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len, int sm_count,
-                      int *split_tokens) {
-    // Cost model: units are dealt round-robin to one persistent CTA per SM,
-    // so the busiest CTA runs ceil(units * groups / SMs) units of ~st
-    // tokens, each with a fixed start-up cost; the partials cost a write in
-    // attend and a read in the merge.  Pick the split count with the
-    // smallest modelled time.
+int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
+                      const int32_t *host_lengths, int sm_count, int *split_tokens) {
     if (sm_count <= 0) sm_count = device_sms();
+    if (host_lengths) {
+        max_len = 0;
+        total_len = 0;
+        for (int r = 0; r < num_requests; ++r) {
+            const int L = host_lengths[r] > 0 ? host_lengths[r] : 0;
+            max_len = L > max_len ? L : max_len;
+            total_len += L;
+        }
+    }
     if (num_requests <= 0 || max_len <= 0) {
-        if (split_tokens) *split_tokens = 1 << 20;
+        if (split_tokens) *split_tokens = max_len > 0 ? max_len : 1;
         return 1;
     }
     if (total_len <= 0) total_len = (int64_t)num_requests * max_len;
     const int rows = qlen * heads;
     const int groups = (rows + 63) / 64;
-    const double bw_sm = 6.5e12 / sm_count;         // bytes/s per SM at the HBM roofline
-    const double t_unit = 1.5e-6;                     // per-unit start-up (query load, epilogue)
+    const double bw_sm = 6.5e12 / sm_count;   // bytes/s per SM at the HBM roofline
+    const double t_tok = MLA_D_QK / bw_sm;     // seconds per KV row on one SM
+    const double t_unit = 1.5e-6;              // per-unit start-up (query load, epilogue)
+    const double t_part_unit = rows * (MLA_D_LATENT * 2.0 + 4.0) * 2.0 / (bw_sm * sm_count);
     const double avg_fill = (double)total_len / ((double)num_requests * max_len);
+    std::vector<double> load;
     int best_ns = 1, best_st = max_len;
     double best_t = 1e30;
     for (int ns = 1; ns <= MLA_MAX_SPLITS; ++ns) {
         const int st = (max_len + ns - 1) / ns;
-        if (st < 64 && ns > 1) break;
-        const double units = std::ceil((double)total_len / st + 0.5 * num_requests * (1.0 - avg_fill));
-        const double per_cta = std::ceil(units * groups / sm_count);
-        const double t_kv = per_cta * (st * (double)MLA_D_QK / bw_sm + t_unit);
-        const double t_part = units * rows * (MLA_D_LATENT * 2.0 + 4.0) * 2.0 / (bw_sm * sm_count);
-        const double t = t_kv + t_part;
+        if (ns > 1 && st < 64) break;
+        double t, units;
+        if (host_lengths) {
+            // exact: walk the units in the kernel's order and deal them out
+            load.assign(sm_count, 0.0);
+            long long u = 0;
+            for (int r = 0; r < num_requests; ++r) {
+                const int L = host_lengths[r] > 0 ? host_lengths[r] : 0;
+                int n = (L + st - 1) / st;
+                n = n < 1 ? 1 : (n > ns ? ns : n);
+                const int b = L / n, m = L % n;
+                for (int k = 0; k < n; ++k)
+                    for (int g = 0; g < groups; ++g, ++u)
+                        load[u % sm_count] += (b + (k < m ? 1 : 0)) * t_tok + t_unit;
+            }
+            units = (double)u / groups;
+            double mx = 0;
+            for (double x : load) mx = x > mx ? x : mx;
+            t = mx;
+        } else {
+            units = std::ceil((double)total_len / st + 0.5 * num_requests * (1.0 - avg_fill));
+            t = std::ceil(units * groups / sm_count) * (st * t_tok + t_unit);
+        }
+        t += units * t_part_unit;
         if (t < best_t * 0.999) {
             best_t = t;
             best_ns = ns;

@@ -81,40 +81,98 @@ struct Params {
 
 // ---------------------------------------------------------------- producer
 
+// One tile of one work unit, as the producer hands it to the consumers.
+struct Tile {
+    int r, k, n_r, base, tok0, ntok, flags;
+    bool valid;
+};
+
+// Iterates this CTA's tiles in order: units u = blockIdx.x, +gridDim.x, ...
+// (each unit row group by row group), each unit cut into TILE-token tiles.
+template <int TILE>
+struct TileIter {
+    UnitCursor cur;
+    long long u;
+    int t, ntiles, start, count, r, k, n_r, base, grp;
+    bool have_unit;
+
+    __device__ void init(const Params &P, int lane) {
+        cur.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, lane);
+        u = (long long)blockIdx.x - gridDim.x;
+        have_unit = false;
+    }
+
+    __device__ Tile next(const Params &P, int lane) {
+        Tile T;
+        T.valid = false;
+        if (!have_unit || t >= ntiles) {
+            u += gridDim.x;
+            int len;
+            if (!cur.find(u / P.row_groups, lane, &r, &k, &n_r, &len, &base)) {
+                have_unit = false;
+                return T;
+            }
+            grp = (int)(u % P.row_groups);
+            split_range(len, n_r, k, &start, &count);
+            ntiles = count > 0 ? (count + TILE - 1) / TILE : 1;
+            t = 0;
+            have_unit = true;
+        }
+        T.valid = true;
+        T.r = r; T.k = k; T.n_r = n_r; T.base = base;
+        T.tok0 = start + t * TILE;
+        T.ntok = count > 0 ? min(TILE, count - t * TILE) : 0;
+        T.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0) | (grp << 8);
+        ++t;
+        return T;
+    }
+};
+
 template <int MT, int TILE>
 __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
+    constexpr int PER_LANE = TILE / 32;
     const int lane = threadIdx.x & 31;
-    UnitCursor cur;
-    cur.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, lane);
-    int it = 0;
-    for (long long u = blockIdx.x;; u += gridDim.x) {
-        long long base_unit = u / P.row_groups;
-        int r, k, n_r, len, base;
-        if (!cur.find(base_unit, lane, &r, &k, &n_r, &len, &base)) break;
-        int start, count;
-        split_range(len, n_r, k, &start, &count);
-        int ntiles = count > 0 ? (count + TILE - 1) / TILE : 1;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = it % kStages;
-            const uint32_t par = ((it / kStages) & 1) ^ 1;
-            if (!mbar_wait(&sm.empty[s], par)) { sm.abort_flag = 1; return; }
-            const int tok0 = start + t * TILE;
-            const int ntok = count > 0 ? min(TILE, count - t * TILE) : 0;
-            if (lane == 0) {
-                Meta m;
-                m.r = r; m.k = k; m.n_r = n_r; m.tok0 = tok0; m.ntok = ntok;
-                m.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0);
-                m.flags |= (int)(u % P.row_groups) << 8;  // row group in the high bits
-                sm.meta[s] = m;
-                mbar_arrive_expect_tx(&sm.full[s], (uint32_t)ntok * MLA_D_QK);
-            }
-            __syncwarp();
-            for (int i = lane; i < ntok; i += 32) {
-                const uint8_t *src = kv_row(P.kv, P.pages, (int64_t)base + tok0 + i, P.pool_rows);
-                bulk_g2s(&sm.kv[s][i * kRowStride], src, MLA_D_QK, &sm.full[s]);
-            }
-            ++it;
+    TileIter<TILE> iter;
+    iter.init(P, lane);
+    // Page indices of a tile are loaded one tile ahead, so their latency
+    // hides behind the wait for a free stage.
+    auto fetch_pages = [&](const Tile &T, int (&pg)[PER_LANE]) {
+#pragma unroll
+        for (int j = 0; j < PER_LANE; ++j) {
+            const int i = lane + 32 * j;
+            pg[j] = (T.valid && i < T.ntok) ? __ldg(P.pages + (int64_t)T.base + T.tok0 + i) : 0;
         }
+    };
+    Tile cur = iter.next(P, lane);
+    int pg[PER_LANE];
+    fetch_pages(cur, pg);
+    int it = 0;
+    while (cur.valid) {
+        Tile nxt = iter.next(P, lane);
+        int npg[PER_LANE];
+        fetch_pages(nxt, npg);
+        const int s = it % kStages;
+        const uint32_t par = ((it / kStages) & 1) ^ 1;
+        if (!mbar_wait(&sm.empty[s], par)) { sm.abort_flag = 1; return; }
+        if (lane == 0) {
+            Meta m;
+            m.r = cur.r; m.k = cur.k; m.n_r = cur.n_r; m.tok0 = cur.tok0; m.ntok = cur.ntok;
+            m.flags = cur.flags;
+            sm.meta[s] = m;
+            mbar_arrive_expect_tx(&sm.full[s], (uint32_t)cur.ntok * MLA_D_QK);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < PER_LANE; ++j) {
+            const int i = lane + 32 * j;
+            if (i < cur.ntok)
+                bulk_g2s(&sm.kv[s][i * kRowStride], kv_row_of_page(P.kv, pg[j], P.pool_rows), MLA_D_QK,
+                         &sm.full[s]);
+        }
+        ++it;
+        cur = nxt;
+#pragma unroll
+        for (int j = 0; j < PER_LANE; ++j) pg[j] = npg[j];
     }
     // Tell the consumers there is no more work.
     const int s = it % kStages;

@@ -216,14 +216,17 @@ __device__ __forceinline__ int request_len(const int32_t *indptr, int r, int64_t
 // page outside [0, pool_rows) flags MLA_DEV_BAD_PAGE and reads row 0
 // instead, so the copy never leaves the pool.  Both the attend kernels and
 // mla_debug_gather address rows through this function.
-__device__ __forceinline__ const uint8_t *kv_row(const uint8_t *kv, const int32_t *pages,
-                                                 int64_t i, int64_t pool_rows) {
-    int64_t p = __ldg(pages + i);
+__device__ __forceinline__ const uint8_t *kv_row_of_page(const uint8_t *kv, int64_t p, int64_t pool_rows) {
     if (p < 0 || p >= pool_rows) {
         flag(MLA_DEV_BAD_PAGE);
         p = 0;
     }
     return kv + p * (int64_t)MLA_D_QK;
+}
+
+__device__ __forceinline__ const uint8_t *kv_row(const uint8_t *kv, const int32_t *pages,
+                                                 int64_t i, int64_t pool_rows) {
+    return kv_row_of_page(kv, __ldg(pages + i), pool_rows);
 }
 
 // Walks the work units (request r, split k), enumerated request-major:

@@ -56,15 +56,35 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const __nv_bfloat16 
                 w = valid ? expf(l - mx) : 0.f;
             }
             tot += w;
+            // Valid splits of this pass, four at a time: their loads are
+            // independent, so they are all in flight together.
             unsigned m = __ballot_sync(0xffffffffu, valid);
             while (m) {
-                const int src = __ffs(m) - 1;
-                m &= m - 1;
-                const float ws = __shfl_sync(0xffffffffu, w, src);
-                const uint4 *p = reinterpret_cast<const uint4 *>(o + ((long long)(kb + src) * nrow + row) * MLA_D_LATENT);
-                const uint4 v0 = __ldg(p + lane), v1 = __ldg(p + 32 + lane);
-                fma8(a0, ws, v0);
-                fma8(a1, ws, v1);
+                int src[4];
+                float ws[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    src[j] = m ? __ffs(m) - 1 : -1;
+                    if (m) m &= m - 1;
+                }
+                uint4 v0[4], v1[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ws[j] = __shfl_sync(0xffffffffu, w, src[j] < 0 ? 0 : src[j]);
+                    if (src[j] >= 0) {
+                        const uint4 *p = reinterpret_cast<const uint4 *>(
+                            o + ((long long)(kb + src[j]) * nrow + row) * MLA_D_LATENT);
+                        v0[j] = __ldg(p + lane);
+                        v1[j] = __ldg(p + 32 + lane);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (src[j] >= 0) {
+                        fma8(a0, ws[j], v0[j]);
+                        fma8(a1, ws[j], v1[j]);
+                    }
+                }
             }
         }
 #pragma unroll

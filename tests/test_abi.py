@@ -100,3 +100,7 @@ def test_choose_splits_plan_is_valid(R, qlen, H, max_len, total):
     assert -(-max_len // st) <= ns          # the longest request fits in ns splits of st tokens
     if max_len * R >= 1 << 20:
         assert ns >= 2                      # long work is split to fill the SMs
+    # with exact host lengths
+    lens = [max_len] + [max(0, (total - max_len) // max(1, R - 1))] * (R - 1)
+    ns2, st2 = mla.choose_splits(R, qlen, H, sm_count=152, lengths=lens)
+    assert 1 <= ns2 <= 256 and -(-max_len // st2) <= ns2

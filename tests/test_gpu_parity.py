@@ -85,7 +85,7 @@ def test_small_workloads_match_oracle(idx, lengths, plan):
     inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
     inp = _to(inp_cpu, DEV)
     if plan == "auto":
-        plan = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, inp.max_len, inp.total_len)
+        plan = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp_cpu.lengths)
     ns, st = plan
     o, lse, latent, lse_m, out = _run_path(inp, ns, st)
     _check_partials(o, lse, inp_cpu, ns, st)
@@ -223,7 +223,7 @@ def _sample_requests(lengths, k=2, seed=0):
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
 def test_full_size_workloads_sampled(idx):
     inp = W.make_inputs(idx, DEV)
-    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, inp.max_len, inp.total_len)
+    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
     _, _, latent, lse_m, out = _run_path(inp, ns, st)
     lens = i32(inp.lengths)
     reqs = _sample_requests(lens, seed=idx)
