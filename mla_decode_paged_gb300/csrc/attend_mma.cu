@@ -12,10 +12,11 @@
 //   * Work units are (request, split) pairs, enumerated request-major and
 //     dealt round-robin to CTAs.  The producer warp walks them with a warp
 //     prefix scan over indptr (no scratch memory, no host round trip).
-//   * For each tile of kTile tokens the producer issues one 576-byte
-//     cp.async.bulk per KV row into a smem stage (row stride 592 bytes, so
-//     both fragment load patterns below are bank-conflict free), completing
-//     on the stage's "full" mbarrier; consumers release it on "empty".
+//   * For each tile of kTile tokens the producer warps issue one 576-byte
+//     cp.async.bulk per KV row (one row per lane, rows spread over 4 warps)
+//     into a smem stage (row stride 592 bytes, so both fragment load
+//     patterns below are bank-conflict free), completing on the stage's
+//     "full" mbarrier; consumers release it on "empty".
 //   * The query rows of all heads x qlen of the request (MQA: they share
 //     every KV row) form the MMA M dimension; a CTA takes up to 16*MT rows
 //     (larger head counts use several row groups, which re-read the same KV
@@ -40,7 +41,11 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+// Several producer warps: a warp issues its bulk copies one lane at a time,
+// so spreading a tile's rows over 4 warps (one row per lane) is what lets
+// random 576-byte rows stream at close to the HBM copy rate.
+constexpr int kProducerWarps = 4;
+constexpr int kThreads = kConsumers + kProducerWarps * 32;
 constexpr int kRowStride = 592;  // smem bytes per KV row (576 + 16)
 constexpr int kQStride = 584;    // f16 elements per query smem row (576 + 8)
 constexpr int kStages = 2;
@@ -130,17 +135,19 @@ struct TileIter {
 
 template <int MT, int TILE>
 __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
-    constexpr int PER_LANE = TILE / 32;
+    constexpr int ROWS = TILE / kProducerWarps;   // rows of a tile this warp copies
+    constexpr int PER_LANE = (ROWS + 31) / 32;
     const int lane = threadIdx.x & 31;
-    TileIter<TILE> iter;
+    const int pw = (threadIdx.x >> 5) - kConsumerWarps;
+    TileIter<TILE> iter;   // every producer warp walks the same tile sequence
     iter.init(P, lane);
     // Page indices of a tile are loaded one tile ahead, so their latency
     // hides behind the wait for a free stage.
     auto fetch_pages = [&](const Tile &T, int (&pg)[PER_LANE]) {
 #pragma unroll
         for (int j = 0; j < PER_LANE; ++j) {
-            const int i = lane + 32 * j;
-            pg[j] = (T.valid && i < T.ntok) ? __ldg(P.pages + (int64_t)T.base + T.tok0 + i) : 0;
+            const int i = pw * ROWS + lane + 32 * j;
+            pg[j] = (T.valid && lane + 32 * j < ROWS && i < T.ntok) ? __ldg(P.pages + (int64_t)T.base + T.tok0 + i) : 0;
         }
     };
     Tile cur = iter.next(P, lane);
@@ -154,19 +161,23 @@ __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
         const int s = it % kStages;
         const uint32_t par = ((it / kStages) & 1) ^ 1;
         if (!mbar_wait(&sm.empty[s], par)) { sm.abort_flag = 1; return; }
+        const int r0 = pw * ROWS;
+        const int mine = max(0, min(ROWS, cur.ntok - r0));
         if (lane == 0) {
-            Meta m;
-            m.r = cur.r; m.k = cur.k; m.n_r = cur.n_r; m.tok0 = cur.tok0; m.ntok = cur.ntok;
-            m.flags = cur.flags;
-            sm.meta[s] = m;
-            mbar_arrive_expect_tx(&sm.full[s], (uint32_t)cur.ntok * MLA_D_QK);
+            if (pw == 0) {
+                Meta m;
+                m.r = cur.r; m.k = cur.k; m.n_r = cur.n_r; m.tok0 = cur.tok0; m.ntok = cur.ntok;
+                m.flags = cur.flags;
+                sm.meta[s] = m;
+            }
+            mbar_arrive_expect_tx(&sm.full[s], (uint32_t)mine * MLA_D_QK);
         }
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < PER_LANE; ++j) {
             const int i = lane + 32 * j;
-            if (i < cur.ntok)
-                bulk_g2s(&sm.kv[s][i * kRowStride], kv_row_of_page(P.kv, pg[j], P.pool_rows), MLA_D_QK,
+            if (i < mine)
+                bulk_g2s(&sm.kv[s][(r0 + i) * kRowStride], kv_row_of_page(P.kv, pg[j], P.pool_rows), MLA_D_QK,
                          &sm.full[s]);
         }
         ++it;
@@ -174,12 +185,12 @@ __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
 #pragma unroll
         for (int j = 0; j < PER_LANE; ++j) pg[j] = npg[j];
     }
-    // Tell the consumers there is no more work.
+    // Tell the consumers there is no more work (every producer warp arrives).
     const int s = it % kStages;
     const uint32_t par = ((it / kStages) & 1) ^ 1;
     if (!mbar_wait(&sm.empty[s], par)) { sm.abort_flag = 1; return; }
     if (lane == 0) {
-        sm.meta[s].flags = kDone;
+        if (pw == 0) sm.meta[s].flags = kDone;
         mbar_arrive(&sm.full[s]);
     }
 }
@@ -451,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_mma_kernel(const Params P)
     const int tid = threadIdx.x;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.full[s], kProducerWarps);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
         sm.abort_flag = 0;
