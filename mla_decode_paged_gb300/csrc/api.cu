@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 #include <vector>
 
@@ -17,6 +18,11 @@ cudaError_t attend_mma_launch(const void *q, int64_t q_row_stride, const void *k
                               int qlen, int heads, float scale, float kv_scale, int num_splits,
                               int split_tokens, void *o, float *lse, int grid, cudaStream_t st);
 cudaError_t attend_mma_status(unsigned int *flags, bool clear);
+cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                             const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
+                             int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
+                             float *lse, int grid, cudaStream_t st);
+cudaError_t attend_tc_status(unsigned int *flags, bool clear);
 cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
                          void *latent, float *lse_out, cudaStream_t st);
 cudaError_t merge_status(unsigned int *flags, bool clear);
@@ -43,6 +49,14 @@ mla_status cuda_fail(cudaError_t e, const char *where) {
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Which attend kernel runs: the tensor-memory (tcgen05) kernel unless the
+// environment variable MLA_ATTEND_KERNEL is "mma" (the warp-MMA kernel),
+// for A/B measurements and tests.
+bool use_warp_mma() {
+    const char *v = std::getenv("MLA_ATTEND_KERNEL");
+    return v && std::string(v) == "mma";
+}
 
 int device_sms() {
     int dev = 0, n = 0;
@@ -75,10 +89,15 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
         !aligned(indptr, 4) || !aligned(pages, 4))
         return fail(MLA_ERR_INVALID, "misaligned pointer (q, kv, o need 16 bytes)");
     if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    if (pool_rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "pool_rows above 2^31 - 1");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
-                                           num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                           split_tokens, o, lse, device_sms(), st);
+    cudaError_t e = use_warp_mma()
+                        ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
+                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
+                                                 split_tokens, o, lse, device_sms(), st)
+                        : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
+                                                num_requests, qlen, heads, scale, kv_scale, num_splits,
+                                                split_tokens, o, lse, device_sms(), st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }
@@ -133,7 +152,7 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
     }
     if (total_len <= 0) total_len = (int64_t)num_requests * max_len;
     const int rows = qlen * heads;
-    const int groups = (rows + 63) / 64;
+    const int groups = use_warp_mma() ? (rows + 63) / 64 : (rows + 47) / 48;
     const double bw_sm = 6.5e12 / sm_count;   // bytes/s per SM at the HBM roofline
     const double t_tok = MLA_D_QK / bw_sm;     // seconds per KV row on one SM
     const double t_unit = 1.5e-6;              // per-unit start-up (query load, epilogue)
@@ -200,7 +219,7 @@ mla_status mla_device_status(void *stream, unsigned int *flags) {
     *flags = 0;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-    cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::merge_status,
+    cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::attend_tc_status, mla::merge_status,
                                                       mla::value_gate_status, mla::gather_status};
     for (auto rd : readers) {
         unsigned int f = 0;

@@ -50,7 +50,7 @@ constexpr int kRowStride = 592;  // smem bytes per KV row (576 + 16)
 constexpr int kQStride = 584;    // f16 elements per query smem row (576 + 8)
 constexpr int kStages = 2;
 
-constexpr unsigned kFirst = 1, kLast = 2, kDone = 4;
+constexpr unsigned kFirst = kTileFirst, kLast = kTileLast, kDone = 4;
 
 struct Meta {
     int r, k, n_r, tok0, ntok, flags;
@@ -86,53 +86,6 @@ struct Params {
 
 // ---------------------------------------------------------------- producer
 
-// One tile of one work unit, as the producer hands it to the consumers.
-struct Tile {
-    int r, k, n_r, base, tok0, ntok, flags;
-    bool valid;
-};
-
-// Iterates this CTA's tiles in order: units u = blockIdx.x, +gridDim.x, ...
-// (each unit row group by row group), each unit cut into TILE-token tiles.
-template <int TILE>
-struct TileIter {
-    UnitCursor cur;
-    long long u;
-    int t, ntiles, start, count, r, k, n_r, base, grp;
-    bool have_unit;
-
-    __device__ void init(const Params &P, int lane) {
-        cur.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, lane);
-        u = (long long)blockIdx.x - gridDim.x;
-        have_unit = false;
-    }
-
-    __device__ Tile next(const Params &P, int lane) {
-        Tile T;
-        T.valid = false;
-        if (!have_unit || t >= ntiles) {
-            u += gridDim.x;
-            int len;
-            if (!cur.find(u / P.row_groups, lane, &r, &k, &n_r, &len, &base)) {
-                have_unit = false;
-                return T;
-            }
-            grp = (int)(u % P.row_groups);
-            split_range(len, n_r, k, &start, &count);
-            ntiles = count > 0 ? (count + TILE - 1) / TILE : 1;
-            t = 0;
-            have_unit = true;
-        }
-        T.valid = true;
-        T.r = r; T.k = k; T.n_r = n_r; T.base = base;
-        T.tok0 = start + t * TILE;
-        T.ntok = count > 0 ? min(TILE, count - t * TILE) : 0;
-        T.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0) | (grp << 8);
-        ++t;
-        return T;
-    }
-};
-
 template <int MT, int TILE>
 __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
     constexpr int ROWS = TILE / kProducerWarps;   // rows of a tile this warp copies
@@ -140,7 +93,7 @@ __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
     const int lane = threadIdx.x & 31;
     const int pw = (threadIdx.x >> 5) - kConsumerWarps;
     TileIter<TILE> iter;   // every producer warp walks the same tile sequence
-    iter.init(P, lane);
+    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
     // Page indices of a tile are loaded one tile ahead, so their latency
     // hides behind the wait for a free stage.
     auto fetch_pages = [&](const Tile &T, int (&pg)[PER_LANE]) {
@@ -150,12 +103,12 @@ __device__ void producer(const Params &P, Smem<MT, TILE> &sm) {
             pg[j] = (T.valid && lane + 32 * j < ROWS && i < T.ntok) ? __ldg(P.pages + (int64_t)T.base + T.tok0 + i) : 0;
         }
     };
-    Tile cur = iter.next(P, lane);
+    Tile cur = iter.next(lane);
     int pg[PER_LANE];
     fetch_pages(cur, pg);
     int it = 0;
     while (cur.valid) {
-        Tile nxt = iter.next(P, lane);
+        Tile nxt = iter.next(lane);
         int npg[PER_LANE];
         fetch_pages(nxt, npg);
         const int s = it % kStages;

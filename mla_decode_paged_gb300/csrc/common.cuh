@@ -295,4 +295,56 @@ struct UnitCursor {
     }
 };
 
+constexpr int kTileFirst = 1, kTileLast = 2;
+
+// One tile of one work unit, as the producer hands it to the consumers.
+struct Tile {
+    int r, k, n_r, base, tok0, ntok, flags;
+    bool valid;
+};
+
+// Iterates this CTA's tiles in order: units u = blockIdx.x, +gridDim.x, ...
+// (each unit row group by row group), each unit cut into TILE-token tiles.
+template <int TILE>
+struct TileIter {
+    UnitCursor cur;
+    long long u;
+    int t, ntiles, start, count, r, k, n_r, base, grp;
+    bool have_unit;
+
+    int row_groups;
+    __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
+                         int groups, int lane) {
+        cur.init(indptr, R, num_pages, num_splits, split_tokens, lane);
+        row_groups = groups;
+        u = (long long)blockIdx.x - gridDim.x;
+        have_unit = false;
+    }
+
+    __device__ Tile next(int lane) {
+        Tile T;
+        T.valid = false;
+        if (!have_unit || t >= ntiles) {
+            u += gridDim.x;
+            int len;
+            if (!cur.find(u / row_groups, lane, &r, &k, &n_r, &len, &base)) {
+                have_unit = false;
+                return T;
+            }
+            grp = (int)(u % row_groups);
+            split_range(len, n_r, k, &start, &count);
+            ntiles = count > 0 ? (count + TILE - 1) / TILE : 1;
+            t = 0;
+            have_unit = true;
+        }
+        T.valid = true;
+        T.r = r; T.k = k; T.n_r = n_r; T.base = base;
+        T.tok0 = start + t * TILE;
+        T.ntok = count > 0 ? min(TILE, count - t * TILE) : 0;
+        T.flags = (t == 0 ? kTileFirst : 0) | (t == ntiles - 1 ? kTileLast : 0) | (grp << 8);
+        ++t;
+        return T;
+    }
+};
+
 }  // namespace mla

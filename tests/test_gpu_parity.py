@@ -23,6 +23,13 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.fixture(params=["tc", "mma"])
+def kernel(request, monkeypatch):
+    """Runs a test once per attend kernel (tensor-memory, warp-MMA)."""
+    monkeypatch.setenv("MLA_ATTEND_KERNEL", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     if not torch.cuda.is_available():
@@ -81,7 +88,7 @@ SMALL = [
 
 @pytest.mark.parametrize("idx,lengths", SMALL)
 @pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (8, 50), (3, 7), "auto"])
-def test_small_workloads_match_oracle(idx, lengths, plan):
+def test_small_workloads_match_oracle(idx, lengths, plan, kernel):
     inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
     inp = _to(inp_cpu, DEV)
     if plan == "auto":
@@ -94,7 +101,7 @@ def test_small_workloads_match_oracle(idx, lengths, plan):
 
 
 @pytest.mark.parametrize("heads,qlen", [(16, 1), (12, 2), (7, 5), (16, 4), (128, 1), (20, 5), (1, 1), (128, 16)])
-def test_row_counts_and_groups(heads, qlen):
+def test_row_counts_and_groups(heads, qlen, kernel):
     """Query-row counts that select each row-tile size and several row groups."""
     spec = W.WorkloadSpec("rows", 11, 3, qlen, heads, heads + (8 if heads < 128 else 0),
                           "fixed:150,40,1", 0.7)
@@ -106,7 +113,7 @@ def test_row_counts_and_groups(heads, qlen):
     _check_full(latent, lse_m, out, inp_cpu)
 
 
-def test_peaky_scores():
+def test_peaky_scores(kernel):
     """A large softmax scale makes attention peaky, so outputs are O(0.1-1)
     and the element-wise bound is tight."""
     inp_cpu = W.make_inputs(0, "cpu")
@@ -119,7 +126,7 @@ def test_peaky_scores():
     _check_full(latent, lse_m, out, inp_cpu)
 
 
-def test_all_requests_empty():
+def test_all_requests_empty(kernel):
     inp_cpu = W.make_inputs(4, "cpu", lengths=[0, 0, 0])
     inp = _to(inp_cpu, DEV)
     o, lse, latent, lse_m, out = _run_path(inp, 4, 16)
@@ -127,7 +134,7 @@ def test_all_requests_empty():
     assert torch.all(latent == 0) and torch.all(out == 0)
 
 
-def test_unused_splits_have_neg_inf_lse():
+def test_unused_splits_have_neg_inf_lse(kernel):
     inp_cpu = W.make_inputs(1, "cpu", lengths=[10, 300])
     inp = _to(inp_cpu, DEV)
     o, lse, *_ = _run_path(inp, 16, 64)
@@ -136,7 +143,7 @@ def test_unused_splits_have_neg_inf_lse():
     assert torch.isfinite(lse[:5, 1]).all() and torch.all(torch.isneginf(lse[5:, 1]))
 
 
-def test_padded_heads_never_read():
+def test_padded_heads_never_read(kernel):
     inp_cpu = W.make_inputs(3, "cpu", lengths=[70, 33])
     assert torch.isnan(inp_cpu.q[:, 96:].float()).all()
     inp = _to(inp_cpu, DEV)
@@ -192,7 +199,7 @@ def test_gather_bit_exact_full_decode_batch():
     assert np.array_equal(u8(rows), ref)
 
 
-def test_bad_pages_and_indptr_are_flagged_not_faulted():
+def test_bad_pages_and_indptr_are_flagged_not_faulted(kernel):
     inp_cpu = W.make_inputs(0, "cpu")
     inp = _to(inp_cpu, DEV)
     bad = inp.pages.clone()
@@ -221,7 +228,7 @@ def _sample_requests(lengths, k=2, seed=0):
 
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_full_size_workloads_sampled(idx):
+def test_full_size_workloads_sampled(idx, kernel):
     inp = W.make_inputs(idx, DEV)
     ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
     _, _, latent, lse_m, out = _run_path(inp, ns, st)
