@@ -46,15 +46,17 @@ constexpr int kT = 128;              // tokens per tile = MMA M
 constexpr int kStages = 2;
 constexpr int kStageBytes = 73728;   // 4 x (16 x 1024) latent + 16 x 512 rope
 constexpr int kRopeOff = 65536;
-constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 7;
+constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarp0 = 9, kProdWarps = 7;
+constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kThreads = (kSoftWarps + 1 + kProdWarps) * 32;
 constexpr int kOps = 160;            // gather4 ops per tile: 32 groups of 4 rows x (4 latent + 1 rope)
-constexpr int kSoftBar = 1;          // named barrier of the softmax warpgroup
+constexpr int kSoftBar = 1;          // named barrier of the two softmax warpgroups
 constexpr float kRebase = 8.f;       // log2 headroom before the reference max moves
 
 template <int NQ>
 struct Cfg {
     static constexpr int NP = 2 * NQ;                      // MMA N (hi and lo terms)
+    static constexpr int HALF = NQ / 2;                    // columns per softmax warpgroup
     static constexpr int OffQ = kStages * kStageBytes;
     static constexpr int QLatBlock = (NP / 8) * 1024;      // one 128-byte column block of Q'
     static constexpr int QRope = 4 * QLatBlock;
@@ -63,8 +65,19 @@ struct Cfg {
     static constexpr uint32_t TmemCols = (10 * NQ <= 256) ? 256 : 512;
 };
 
+// Descriptor of the tile in a stage (and of the tile after it), written by
+// producer warp 0 before it arrives on the stage's full barrier, so the
+// MMA and softmax roles read the work sequence instead of walking indptr.
+struct TileMeta {
+    int r, k, n_r, ntok, flags;         // flags: kTileFirst / kTileLast / kMetaDone, row group << 8
+    int nxt_r, nxt_ntok, nxt_flags;     // nxt_flags = 0: no next tile
+};
+constexpr int kMetaDone = 4, kNxtValid = 16;
+
 template <int NQ>
 struct Misc {
+    TileMeta meta[kStages];
+    int64_t orow[NQ];       // o row (element offset / 512) of each query column, -1 for padding
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full, p_full, q_ready, o_done, fin;
     uint32_t tmem;
@@ -73,7 +86,7 @@ struct Misc {
     float m[NQ];            // reference max of the row, log2 domain
     float alpha[NQ];
     float invl[NQ];
-    float red[kSoftWarps][NQ];
+    float red[4][NQ];       // per TMEM lane quarter
 };
 
 struct Params {
@@ -104,6 +117,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t par, int *
     return true;
 }
 
+// N consecutive f32 TMEM columns (N a multiple of 8) of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c < N; c += 8) {
+        uint32_t r[8];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr + c));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[c + i] = __uint_as_float(r[i]);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&v)[N]) {
+#pragma unroll
+    for (int c = 0; c < N; c += 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr + c),
+                     "r"(__float_as_uint(v[c])), "r"(__float_as_uint(v[c + 1])), "r"(__float_as_uint(v[c + 2])),
+                     "r"(__float_as_uint(v[c + 3])), "r"(__float_as_uint(v[c + 4])), "r"(__float_as_uint(v[c + 5])),
+                     "r"(__float_as_uint(v[c + 6])), "r"(__float_as_uint(v[c + 7]))
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ producers
 
 template <int NQ>
@@ -131,6 +170,7 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
     Tile cur = iter.next(lane);
     int rows[4];
     fetch(cur, rows);
+    int n_issued = 0;
     for (int it = 0; cur.valid; ++it) {
         Tile nxt = iter.next(lane);
         int nrows[4];
@@ -141,7 +181,15 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
         uint32_t bytes = issue ? (part < 4 ? 512u : 256u) : 0u;
 #pragma unroll
         for (int d = 16; d; d >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, d);
-        if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[s], bytes);
+        if (lane == 0) {
+            if (pw == 0) {
+                TileMeta m;
+                m.r = cur.r; m.k = cur.k; m.n_r = cur.n_r; m.ntok = cur.ntok; m.flags = cur.flags;
+                m.nxt_r = nxt.r; m.nxt_ntok = nxt.ntok; m.nxt_flags = nxt.valid ? (nxt.flags | kNxtValid) : 0;
+                ms.meta[s] = m;
+            }
+            mbar_arrive_expect_tx(&ms.kv_full[s], bytes);
+        }
         __syncwarp();
         if (issue) {
             uint8_t *st = sm + s * kStageBytes;
@@ -156,11 +204,22 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
         cur = nxt;
 #pragma unroll
         for (int i = 0; i < 4; ++i) rows[i] = nrows[i];
+        n_issued = it + 1;
+    }
+    // No more work: one last "done" descriptor through the next stage.
+    const int s2 = n_issued % kStages;
+    if (!wait_or_abort(&ms.kv_empty[s2], ((n_issued / kStages) & 1) ^ 1, &ms.abort_flag)) return;
+    if (lane == 0) {
+        if (pw == 0) ms.meta[s2].flags = kMetaDone;
+        mbar_arrive(&ms.kv_full[s2]);
     }
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
+// Per tile, in order: QK^T (18 MMAs into S), then -- once the softmax has
+// written P' -- P.V (16 MMAs, latent blocks interleaved so consecutive MMAs
+// feed different accumulators).  A stage is held only for its own tile.
 template <int NQ>
 __device__ void mma_issuer(const Params &P, uint8_t *sm) {
     using C = Cfg<NQ>;
@@ -170,21 +229,25 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
     const uint32_t tm = ms.tmem;
     constexpr uint32_t kIdQK = tc::idesc_e4m3(C::NP, false, false);
     constexpr uint32_t kIdPV = tc::idesc_e4m3(C::NP, true, true);
-    TileIter<kT> iter;
-    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
-    int n_tiles = 0, n_units = 0;
+    int n_p = 0, n_units = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
-        const Tile T = iter.next(lane);
-        if (!T.valid) break;
         const int s = it % kStages;
         if (!(ok = wait_or_abort(&ms.kv_full[s], (it / kStages) & 1, &ms.abort_flag))) break;
-        if (T.ntok == 0) {  // empty request: nothing to multiply
+        const TileMeta M = ms.meta[s];
+        if (M.flags & kMetaDone) break;
+        if (M.ntok == 0) {
+            // Empty request: nothing to multiply; release the stage once the
+            // softmax has read its descriptor.
+            if (!(ok = wait_or_abort(&ms.p_full, (n_p++) & 1, &ms.abort_flag))) break;
             if (lane == 0) mbar_arrive(&ms.kv_empty[s]);
             continue;
         }
-        const bool first = T.flags & kTileFirst;
-        if (first && !(ok = wait_or_abort(&ms.q_ready, n_units & 1, &ms.abort_flag))) break;
+        const bool first = M.flags & kTileFirst;
+        if (first) {
+            if (!(ok = wait_or_abort(&ms.q_ready, n_units & 1, &ms.abort_flag))) break;
+            ++n_units;
+        }
         tc::fence_after();
         const uint32_t st = base + s * kStageBytes;
         if (lane == 0) {
@@ -201,22 +264,20 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
             tc::commit(&ms.s_full);
         }
         __syncwarp();
-        if (!(ok = wait_or_abort(&ms.p_full, n_tiles & 1, &ms.abort_flag))) break;
+        if (!(ok = wait_or_abort(&ms.p_full, (n_p++) & 1, &ms.abort_flag))) break;
         tc::fence_after();
         if (lane == 0) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int b = 0; b < 4; ++b)
                     tc::mma_e4m3(tm + C::NP * (1 + b), tc::sdesc(st + b * 16384 + kk * 4096, 16384, 1024, tc::kSw128),
                                  tc::sdesc(base + C::OffP + kk * 4096, 16384, 1024, tc::kSw128), kIdPV,
                                  !(first && kk == 0));
             tc::commit(&ms.kv_empty[s]);
-            if (T.flags & kTileLast) tc::commit(&ms.o_done);
+            if (M.flags & kTileLast) tc::commit(&ms.o_done);
         }
         __syncwarp();
-        ++n_tiles;
-        if (first) ++n_units;
     }
     // Every MMA issued so far must be complete before TMEM is released.
     if (lane == 0) tc::commit(&ms.fin);
@@ -229,37 +290,37 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
 // The query rows of tile T's request and row group as the B operand Q':
 // row n = q_n * 2^e_n rounded to e4m3 (hi), row NQ + n = 16 * (q_n * 2^e_n
 // - hi) rounded to e4m3 (lo), in the K-major 128B / 64B swizzled layouts;
-// c[n] = scale * kv_scale * log2(e) / 2^e_n.
+// c[n] = scale * kv_scale * log2(e) / 2^e_n.  Run by the 8 softmax warps.
 template <int NQ>
-__device__ void prep_query(const Params &P, uint8_t *sm, const Tile &T) {
+__device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
     using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rows_total = P.qlen * P.heads, grp = T.flags >> 8;
-    constexpr int kPerWarp = NQ / kSoftWarps;
+    const int rows_total = P.qlen * P.heads;
+    constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6
 #pragma unroll 1
-    for (int i0 = 0; i0 < kPerWarp; i0 += 4) {
-        uint4 v[4][3];
-        bool valid[4];
+    for (int i0 = 0; i0 < kPerWarp; i0 += 2) {
+        uint4 v[2][3];
+        bool valid[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             const int rho = grp * NQ + n;
-            valid[i] = (i0 + i < kPerWarp) && rho < rows_total;
+            valid[i] = rho < rows_total;
             const __nv_bfloat16 *src = P.q;
             if (valid[i]) {
                 const int tq = rho / P.heads, h = rho % P.heads;
-                src = P.q + ((int64_t)T.r * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK;
+                src = P.q + ((int64_t)req * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK;
             }
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 const int ch = lane + 32 * j;
-                v[i][j] = (valid[i] && ch < 72) ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
+                v[i][j] = (valid[i] && ch < 72) ? __ldg(reinterpret_cast<const uint4 *>(src) + ch)
+                                                : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (i0 + i >= kPerWarp) break;
+        for (int i = 0; i < 2; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             float amax = 0.f;
 #pragma unroll
@@ -290,8 +351,7 @@ __device__ void prep_query(const Params &P, uint8_t *sm, const Tile &T) {
                     const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
                     const float2 r = make_float2((x.x - hf.x) * 16.f, (x.y - hf.y) * 16.f);
                     const __nv_fp8x2_storage_t l8 = __nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
-                    const int sh = (e2 & 1) * 16;
-                    if (sh == 0) {
+                    if ((e2 & 1) == 0) {
                         hi[e2 >> 1] = h8;
                         lo[e2 >> 1] = l8;
                     } else {
@@ -316,200 +376,214 @@ __device__ void prep_query(const Params &P, uint8_t *sm, const Tile &T) {
         }
     }
     tc::fence_async_smem();   // generic-proxy writes -> tensor-core reads
-    named_sync(kSoftBar, kSoftWarps * 32);
+    named_sync(kSoftBar, kSoftThreads);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms.q_ready);
 }
 
+// Softmax warpgroups: thread (warpgroup g, TMEM lane t) owns token t of the
+// tile (latent row t of O in the epilogue) and query columns
+// [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale), c/16 and
+// the reference max m in registers.  The tile sequence comes from the
+// stage descriptors.
 template <int NQ>
 __device__ void softmax(const Params &P, uint8_t *sm) {
     using C = Cfg<NQ>;
+    constexpr int H2 = C::HALF;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t tm = ms.tmem + ((uint32_t)(warp * 32) << 16);
+    const int wq = warp & 3, t = tid & 127, n0 = (warp >> 2) * H2;
+    const uint32_t tm = ms.tmem + ((uint32_t)(wq * 32) << 16);
     const int S = P.R * P.qlen, rows_total = P.qlen * P.heads;
-    TileIter<kT> iter;
-    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
-    Tile cur = iter.next(lane);
-    Tile nxt = iter.next(lane);
-    if (cur.valid && cur.ntok > 0) {
-        prep_query<NQ>(P, sm, cur);
-        if (lane == 0) mbar_arrive(&ms.q_ready);
-    }
-    float l[NQ];
-    int n_tiles = 0, n_units = 0;
-    while (cur.valid) {
-        const int grp = cur.flags >> 8;
-        if (cur.ntok == 0) {
+    float l[H2], cr[H2], c16[H2], mr[H2];
+    int n_s = 0, n_units = 0;
+    uint8_t *prow = sm + C::OffP + (t >> 3) * 1024 + (t & 7) * 128;
+    for (int it = 0;; ++it) {
+        const int s = it % kStages;
+        if (!wait_or_abort(&ms.kv_full[s], (it / kStages) & 1, &ms.abort_flag)) return;
+        const TileMeta M = ms.meta[s];
+        if (M.flags & kMetaDone) return;
+        const int grp = M.flags >> 8;
+        const bool first = M.flags & kTileFirst, last = M.flags & kTileLast;
+        // The very first unit's query: prepared here; later ones at the end
+        // of the unit before them.
+        if (it == 0 && M.ntok > 0) prep_query<NQ>(P, sm, M.r, grp);
+        const bool next_unit = (M.nxt_flags & kNxtValid) && M.nxt_ntok > 0 && last;
+        if (M.ntok == 0) {
             // Empty request: LSE -inf for its rows and every split.
-            for (int i = tid; i < NQ * P.num_splits; i += kSoftWarps * 32) {
+            for (int i = tid; i < NQ * P.num_splits; i += kSoftThreads) {
                 const int n = i % NQ, k = i / NQ, rho = grp * NQ + n;
                 if (rho < rows_total) {
-                    const int64_t t = (int64_t)cur.r * P.qlen + rho / P.heads;
-                    P.lse[((int64_t)k * S + t) * P.heads + rho % P.heads] = -INFINITY;
+                    const int64_t tt = (int64_t)M.r * P.qlen + rho / P.heads;
+                    P.lse[((int64_t)k * S + tt) * P.heads + rho % P.heads] = -INFINITY;
                 }
             }
-            if (nxt.valid && nxt.ntok > 0) {   // nxt is the first tile of a new unit
-                prep_query<NQ>(P, sm, nxt);
-                if (lane == 0) mbar_arrive(&ms.q_ready);
-            }
-            cur = nxt;
-            nxt = iter.next(lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full);   // descriptor read: the stage may be released
+            if (next_unit) prep_query<NQ>(P, sm, M.nxt_r, M.nxt_flags >> 8);
             continue;
         }
-        const bool first = cur.flags & kTileFirst, last = cur.flags & kTileLast;
         if (first) {
+            // c[] of this unit was published by prep_query's barrier.
 #pragma unroll
-            for (int n = 0; n < NQ; ++n) l[n] = 0.f;
-            if (tid < NQ) ms.m[tid] = -INFINITY;
-        }
-        // ---- scores of this thread's token
-        if (!wait_or_abort(&ms.s_full, n_tiles & 1, &ms.abort_flag)) return;
-        tc::fence_after();
-        named_sync(kSoftBar, kSoftWarps * 32);   // m[] initialised, c[] of this unit visible
-        float s[NQ];
-#pragma unroll
-        for (int c0 = 0; c0 < NQ; c0 += 16) {
-            float hi[16], lo[16];
-            tc::ld16(tm + c0, hi);
-            tc::ld16(tm + NQ + c0, lo);
-            tc::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s[c0 + j] = (hi[j] + lo[j] * 0.0625f) * ms.c[c0 + j];
-        }
-        const bool live = tid < cur.ntok;
-#pragma unroll
-        for (int n = 0; n < NQ; ++n) s[n] = live ? s[n] : -INFINITY;
-        // ---- lazy reference max
-        bool over = false;
-#pragma unroll
-        for (int n = 0; n < NQ; ++n) over |= s[n] > ms.m[n] + kRebase;
-        if (tc::bar_any(kSoftBar, kSoftWarps * 32, over)) {
-#pragma unroll
-            for (int n = 0; n < NQ; ++n) {
-                float v = s[n];
-#pragma unroll
-                for (int d = 16; d; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
-                if (lane == 0) ms.red[warp][n] = v;
+            for (int j = 0; j < H2; ++j) {
+                l[j] = 0.f;
+                cr[j] = ms.c[n0 + j];
+                c16[j] = cr[j] * 0.0625f;
+                mr[j] = -INFINITY;
             }
-            named_sync(kSoftBar, kSoftWarps * 32);
             if (tid < NQ) {
-                const float mo = ms.m[tid];
+                const int rho = grp * NQ + tid;
+                ms.orow[tid] = rho < rows_total
+                                   ? ((int64_t)M.k * S + (int64_t)M.r * P.qlen + rho / P.heads) * P.heads + rho % P.heads
+                                   : -1;
+            }
+        }
+        // ---- scores (log2 domain) of this thread's token and columns
+        if (!wait_or_abort(&ms.s_full, n_s & 1, &ms.abort_flag)) return;
+        ++n_s;
+        tc::fence_after();
+        float sc[H2];
+        bool over = false;
+        {
+            float hi[H2], lo[H2];
+            ld_cols<H2>(tm + n0, hi);
+            ld_cols<H2>(tm + NQ + n0, lo);
+            tc::wait_ld();
+            const bool live = t < M.ntok;
+#pragma unroll
+            for (int j = 0; j < H2; ++j) {
+                sc[j] = live ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                over |= sc[j] - mr[j] > kRebase;   // also true for every live token while m = -inf
+            }
+        }
+        // ---- lazy reference max (rare after a unit's first tile)
+        if (tc::bar_any(kSoftBar, kSoftThreads, over)) {
+#pragma unroll
+            for (int j = 0; j < H2; ++j) {
+                float v = sc[j];
+#pragma unroll
+                for (int dd = 16; dd; dd >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, dd));
+                if (lane == 0) ms.red[wq][n0 + j] = v;
+            }
+            named_sync(kSoftBar, kSoftThreads);
+            if (tid < NQ) {
+                const float mo = first ? -INFINITY : ms.m[tid];
                 float mn = fmaxf(fmaxf(ms.red[0][tid], ms.red[1][tid]), fmaxf(ms.red[2][tid], ms.red[3][tid]));
                 mn = fmaxf(mn, mo);
                 ms.alpha[tid] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
                 ms.m[tid] = mn;
             }
-            named_sync(kSoftBar, kSoftWarps * 32);
+            named_sync(kSoftBar, kSoftThreads);
 #pragma unroll
-            for (int n = 0; n < NQ; ++n) l[n] *= ms.alpha[n];
+            for (int j = 0; j < H2; ++j) {
+                mr[j] = ms.m[n0 + j];
+                l[j] *= ms.alpha[n0 + j];
+            }
             if (!first) {
-                // O holds earlier tiles of this unit (the PV before this QK is
-                // complete): scale its hi and lo columns of every latent block.
+                // O holds this unit's earlier tiles (their P.V is complete:
+                // this tile's QK^T was issued after it): scale this
+                // warpgroup's hi and lo columns of every latent block.
 #pragma unroll 1
                 for (int b = 0; b < 4; ++b) {
-#pragma unroll
-                    for (int c0 = 0; c0 < C::NP; c0 += 16) {
-                        float v[16];
-                        const uint32_t addr = tm + C::NP * (1 + b) + c0;
-                        tc::ld16(addr, v);
+#pragma unroll 1
+                    for (int part = 0; part < 2; ++part) {
+                        float v[H2];
+                        const uint32_t addr = tm + C::NP * (1 + b) + part * NQ + n0;
+                        ld_cols<H2>(addr, v);
                         tc::wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] *= ms.alpha[(c0 + j) % NQ];
-                        tc::st16(addr, v);
+                        for (int j = 0; j < H2; ++j) v[j] *= ms.alpha[n0 + j];
+                        st_cols<H2>(addr, v);
                     }
                 }
                 tc::wait_st();
             }
         }
-        // ---- P' = hi + lo/16 of p = 2^(s - m) (<= 2^8), row `tid` of P'^T,
-        // written 16 columns at a time (hi chunk c, lo chunk NQ/16 + c)
-        uint8_t *prow = sm + C::OffP + (tid >> 3) * 1024 + (tid & 7) * 128;
+        // ---- P' = hi + lo/16 of p = 2^(s - m) (<= 2^8): hi = p rounded to 3
+        // mantissa bits in fp32 (exact in e4m3), lo = 16 * (p - hi); this
+        // thread's bytes of row t of P'^T
+        uint32_t ph[H2 / 4], pl[H2 / 4];
 #pragma unroll
-        for (int c0 = 0; c0 < NQ; c0 += 16) {
-            uint32_t ph[4], pl[4];
+        for (int j = 0; j < H2; j += 2) {
+            float hv[2], lv[2];
 #pragma unroll
-            for (int n = c0; n < c0 + 16; n += 2) {
-                const float p0 = exp2f(s[n] - ms.m[n]), p1 = exp2f(s[n + 1] - ms.m[n + 1]);
-                l[n] += p0;
-                l[n + 1] += p1;
-                const __nv_fp8x2_storage_t h8 =
-                    __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3);
-                const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                const __nv_fp8x2_storage_t l8 = __nv_cvt_float2_to_fp8x2(
-                    make_float2((p0 - hf.x) * 16.f, (p1 - hf.y) * 16.f), __NV_SATFINITE, __NV_E4M3);
-                const int wi = (n - c0) >> 2, sh = (n & 2) * 8;
-                ph[wi] = (sh ? ph[wi] : 0u) | ((uint32_t)h8 << sh);
-                pl[wi] = (sh ? pl[wi] : 0u) | ((uint32_t)l8 << sh);
+            for (int e = 0; e < 2; ++e) {
+                const float pv = exp2f(sc[j + e] - mr[j + e]);
+                l[j + e] += pv;
+                hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
+                lv[e] = (pv - hv[e]) * 16.f;
             }
-            const int ch = c0 >> 4, cl = (NQ >> 4) + ch;
-            *reinterpret_cast<uint4 *>(prow + (((ch ^ tid) & 7) << 4)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-            *reinterpret_cast<uint4 *>(prow + (((cl ^ tid) & 7) << 4)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            const uint32_t h8 = __nv_cvt_float2_to_fp8x2(make_float2(hv[0], hv[1]), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t l8 = __nv_cvt_float2_to_fp8x2(make_float2(lv[0], lv[1]), __NV_SATFINITE, __NV_E4M3);
+            const int wi = j >> 2;
+            if ((j & 2) == 0) {
+                ph[wi] = h8;
+                pl[wi] = l8;
+            } else {
+                ph[wi] |= h8 << 16;
+                pl[wi] |= l8 << 16;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < H2 / 8; ++g) {
+            const int bh = n0 + 8 * g, bl = NQ + n0 + 8 * g;   // byte offsets in the 128-byte row
+            *reinterpret_cast<uint2 *>(prow + ((((bh >> 4) ^ t) & 7) << 4) + (bh & 15)) = make_uint2(ph[2 * g], ph[2 * g + 1]);
+            *reinterpret_cast<uint2 *>(prow + ((((bl >> 4) ^ t) & 7) << 4) + (bl & 15)) = make_uint2(pl[2 * g], pl[2 * g + 1]);
         }
         tc::fence_async_smem();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms.p_full);
-        ++n_tiles;
-        // QK of the unit's last tile is complete: refill the query buffer
-        // for the next unit while the tensor cores run this tile's PV.
-        if (last && nxt.valid && nxt.ntok > 0) {
-            named_sync(kSoftBar, kSoftWarps * 32);   // every thread is done with c[]
-            prep_query<NQ>(P, sm, nxt);
-            if (lane == 0) mbar_arrive(&ms.q_ready);
-        }
-
         if (last) {
+            // Refill the query buffer for the next unit (its QK^T may start
+            // once this tile's P.V has been issued).
+            if (next_unit) prep_query<NQ>(P, sm, M.nxt_r, M.nxt_flags >> 8);
             // ---- unit epilogue: row sums, o, lse
 #pragma unroll
-            for (int n = 0; n < NQ; ++n) {
-                float v = l[n];
+            for (int j = 0; j < H2; ++j) {
+                float v = l[j];
 #pragma unroll
-                for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-                if (lane == 0) ms.red[warp][n] = v;
+                for (int dd = 16; dd; dd >>= 1) v += __shfl_xor_sync(0xffffffffu, v, dd);
+                if (lane == 0) {
+                    ms.red[wq][n0 + j] = v;
+                    if (wq == 0) ms.m[n0 + j] = mr[j];
+                }
             }
             if (!wait_or_abort(&ms.o_done, n_units & 1, &ms.abort_flag)) return;
             tc::fence_after();
-            named_sync(kSoftBar, kSoftWarps * 32);
+            named_sync(kSoftBar, kSoftThreads);
             if (tid < NQ) {
                 const float lt = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
                 ms.invl[tid] = P.kv_scale / lt;
-                const int rho = grp * NQ + tid;
-                if (rho < rows_total) {
-                    const int64_t t = (int64_t)cur.r * P.qlen + rho / P.heads;
-                    const int h = rho % P.heads;
-                    P.lse[((int64_t)cur.k * S + t) * P.heads + h] = (ms.m[tid] + __log2f(lt)) * 0.69314718055994531f;
-                    if (cur.k == cur.n_r - 1)
-                        for (int k2 = cur.k + 1; k2 < P.num_splits; ++k2)
-                            P.lse[((int64_t)k2 * S + t) * P.heads + h] = -INFINITY;
-                }
-            }
-            named_sync(kSoftBar, kSoftWarps * 32);
-#pragma unroll 1
-            for (int b = 0; b < 4; ++b) {
-#pragma unroll
-                for (int c0 = 0; c0 < NQ; c0 += 16) {
-                    float hi[16], lo[16];
-                    tc::ld16(tm + C::NP * (1 + b) + c0, hi);
-                    tc::ld16(tm + C::NP * (1 + b) + NQ + c0, lo);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = c0 + j, rho = grp * NQ + n;
-                        if (rho < rows_total) {
-                            const int64_t t = (int64_t)cur.r * P.qlen + rho / P.heads;
-                            const int64_t orow = ((int64_t)cur.k * S + t) * P.heads + rho % P.heads;
-                            P.o[orow * MLA_D_LATENT + 128 * b + tid] =
-                                __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * ms.invl[n]);
-                        }
+                const int64_t orow = ms.orow[tid];
+                if (orow >= 0) {
+                    P.lse[orow] = (ms.m[tid] + __log2f(lt)) * 0.69314718055994531f;
+                    if (M.k == M.n_r - 1) {
+                        const int64_t step = (int64_t)S * P.heads;
+                        for (int k2 = M.k + 1; k2 < P.num_splits; ++k2) P.lse[orow + (k2 - M.k) * step] = -INFINITY;
                     }
                 }
             }
+            named_sync(kSoftBar, kSoftThreads);
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                float hi[H2], lo[H2];
+                ld_cols<H2>(tm + C::NP * (1 + b) + n0, hi);
+                ld_cols<H2>(tm + C::NP * (1 + b) + NQ + n0, lo);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < H2; ++j) {
+                    const int64_t orow = ms.orow[n0 + j];
+                    if (orow >= 0)
+                        P.o[orow * MLA_D_LATENT + 128 * b + t] =
+                            __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * ms.invl[n0 + j]);
+                }
+            }
             tc::fence_before();
-            named_sync(kSoftBar, kSoftWarps * 32);
+            named_sync(kSoftBar, kSoftThreads);
             ++n_units;
         }
-        cur = nxt;
-        nxt = iter.next(lane);
     }
 }
 
@@ -537,14 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    // Register split (per warpgroup, 384 x 168 at launch): the softmax
-    // warpgroup holds two NQ-wide rows per thread, the others little.
-    // 128 x 232 + 256 x 104 = 56320 <= 64512.
+    // Register split (per warpgroup; 512 x 128 at launch): the two softmax
+    // warpgroups take 184, the MMA / producer warpgroups 72.
+    // 256 x 184 + 256 x 72 = 65536.
     if (warp < kSoftWarps) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
         softmax<NQ>(P, sm);
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
         if (warp == kMmaWarp) mma_issuer<NQ>(P, sm);
         else producer<NQ>(P, &mlat, &mrope, sm);
     }
@@ -605,10 +679,10 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
     cuuint32_t box_lat[2] = {128, 1}, box_rope[2] = {64, 1}, es[2] = {1, 1};
     void *base = const_cast<void *>(kv);
     if (enc(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_lat, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
             CUDA_SUCCESS ||
         enc(&mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_rope, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
             CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     Params P;
