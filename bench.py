@@ -52,6 +52,22 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of per-rank floats across the process group (the
+    slowest rank's times); identity without one."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def aggregate_value(rows_per_step, steps, world_size, max_seconds):
+    """Whole-job throughput: query rows of every rank over the slowest rank's time."""
+    return rows_per_step * steps * world_size / max_seconds
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -237,10 +253,7 @@ def run_gpu(args):
     ok = torch.equal(out_h, out.cpu())
 
     if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total, e2e_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total, e2e_total = float(t[0]), float(t[1])
+        total, e2e_total = max_over_ranks([total, e2e_total], dev)
     if rank != 0:
         return None
 
@@ -250,7 +263,7 @@ def run_gpu(args):
     traffic = _ncu_traffic(spec.name)
     rec = {
         "metric": METRIC,
-        "value": S * args.steps * ws / total,
+        "value": aggregate_value(S, args.steps, ws, total),
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
@@ -278,7 +291,7 @@ def run_gpu(args):
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "algorithmic_bytes_per_launch": stats["attend_bytes"], "traffic": traffic,
         },
-        "e2e": {"value": S * args.steps * ws / e2e_total, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": aggregate_value(S, args.steps, ws, e2e_total), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "output_matches_device": bool(ok)},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
@@ -289,15 +302,26 @@ def run_gpu(args):
 
 
 def _ncu_traffic(workload):
-    """DRAM bytes per attend launch from the committed ncu summary of the
-    current kernel, if one exists for this workload (else null)."""
-    p = os.path.join(ROOT, "profiles", "attend_%s_traffic.json" % workload)
-    if os.path.exists(p):
-        with open(p) as f:
-            d = json.load(f)
-        if d.get("current", True):
-            return d.get("dram_bytes_per_launch")
-    return None
+    """DRAM bytes per attend launch from the committed ncu summary of this
+    workload, if its kernel-source hash matches the current sources (else
+    null: the counters describe an older kernel)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "attend_tc_%s.md" % workload)
+    if not os.path.exists(p) or os.environ.get("MLA_ATTEND_KERNEL") == "mma":
+        return None
+    vals = {}
+    for line in open(p):
+        line = line.strip()
+        if ":" in line and line.split(":")[0] in ("kernel_sources_sha256_16", "dram_bytes_per_launch"):
+            k, v = line.split(":", 1)
+            vals[k] = v.strip()
+    h = hashlib.sha256()
+    for f in ("attend_tc.cu", "tc.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "mla_decode_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if vals.get("kernel_sources_sha256_16") != h.hexdigest()[:16]:
+        return None
+    return int(vals["dram_bytes_per_launch"])
 
 
 def cpu_baseline(spec, inp, budget_s=15.0):
