@@ -143,6 +143,26 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
                           void *out, void *stream);
 
 /*
+ * mla_merge_value_gate -- mla_merge_splits followed by mla_value_gate in one
+ * launch: the merged latent is formed in shared memory (rounded to bf16, as
+ * the two-call path rounds it) and projected and gated without a round trip
+ * through global memory.
+ *
+ * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
+ * m1c_inputs / post (the LSE merge of the splits, then W_UV and the gate)
+ * and vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value,
+ * MlaValue / MlaGate (projection, rounding and gating as in mla_value_gate).
+ *
+ *   o, lse, num_splits   as mla_merge_splits (rows = num_requests * qlen)
+ *   w_uv, gate, lengths  as mla_value_gate;  out bf16 [S, heads*128] (written)
+ *   latent, lse_out      optional (may be NULL): the merged latent
+ *                        bf16 [S, heads, 512] and LSE f32 [S, heads]
+ */
+mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits, const void *w_uv,
+                                const void *gate, const int32_t *lengths, int num_requests, int qlen,
+                                int heads, void *out, void *latent, float *lse_out, void *stream);
+
+/*
  * mla_choose_splits -- a split plan for mla_decode_attend from host-known
  * sizes (no device read).  Returns num_splits (>= 1) and writes
  * *split_tokens.  The plan minimises a model of the attend time: work units

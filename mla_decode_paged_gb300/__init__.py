@@ -28,7 +28,7 @@ D_QK, D_LATENT, D_V = 576, 512, 128
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
 
-__all__ = ["attend", "merge", "value_gate", "decode_step", "choose_splits", "debug_gather",
+__all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "debug_gather",
            "device_status", "build", "library", "MlaError"]
 
 
@@ -64,10 +64,11 @@ def library() -> ctypes.CDLL:
                                       vp, vp, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
+    lib.mla_merge_value_gate.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
-    for name in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate", "mla_debug_gather",
+    for name in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
                  "mla_device_status", "mla_choose_splits"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -175,6 +176,36 @@ def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
     st = library().mla_value_gate(_ptr(latent), _ptr(w_uv), _ptr(gate), _ptr(lengths), lengths.numel(), qlen,
                                   H, _ptr(out), ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_value_gate")
+    return out
+
+
+def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=None, lse_out=None,
+                     stream=None):
+    """Merge + W_UV + gate in one launch: returns ``out [S, heads*128] bf16``.
+    ``latent`` / ``lse_out`` (optional tensors) also receive the merged
+    latent and LSE."""
+    _need(o.dtype == torch.bfloat16 and o.dim() == 4 and o.shape[3] == D_LATENT and o.is_contiguous(),
+          "o must be contiguous bf16 [splits, S, heads, 512]")
+    _need(lse.dtype == torch.float32 and lse.shape == o.shape[:3] and lse.is_contiguous(),
+          "lse must be contiguous f32 [splits, S, heads]")
+    ns, S, H = o.shape[:3]
+    _need(w_uv.dtype == torch.bfloat16 and tuple(w_uv.shape) == (H, D_V, D_LATENT) and w_uv.is_contiguous(),
+          "w_uv must be contiguous bf16 [heads, 128, 512]")
+    _need(gate.dtype == torch.bfloat16 and tuple(gate.shape) == (S, H * D_V) and gate.is_contiguous(),
+          "gate must be contiguous bf16 [S, heads*128]")
+    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S, "lengths must be int32 [S / qlen]")
+    if latent is not None:
+        _need(latent.dtype == torch.bfloat16 and tuple(latent.shape) == (S, H, D_LATENT) and latent.is_contiguous(),
+              "latent must be contiguous bf16 [S, heads, 512]")
+    if lse_out is not None:
+        _need(lse_out.dtype == torch.float32 and tuple(lse_out.shape) == (S, H) and lse_out.is_contiguous(),
+              "lse_out must be contiguous f32 [S, heads]")
+    if out is None:
+        out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=o.device)
+    st = library().mla_merge_value_gate(_ptr(o), _ptr(lse), ns, _ptr(w_uv), _ptr(gate), _ptr(lengths),
+                                        lengths.numel(), qlen, H, _ptr(out), _ptr(latent), _ptr(lse_out),
+                                        ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_merge_value_gate")
     return out
 
 

@@ -29,6 +29,10 @@ cudaError_t merge_status(unsigned int *flags, bool clear);
 cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *gate,
                               const int32_t *lengths, int R, int qlen, int H, void *out, cudaStream_t st);
 cudaError_t value_gate_status(unsigned int *flags, bool clear);
+cudaError_t merge_value_launch(const void *o, const float *lse, int num_splits, const void *w_uv, const void *gate,
+                               const int32_t *lengths, int R, int qlen, int H, void *out, void *latent,
+                               float *lse_out, int sms, cudaStream_t st);
+cudaError_t merge_value_status(unsigned int *flags, bool clear);
 cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
                           int R, int64_t total_rows, void *out, cudaStream_t st);
 cudaError_t gather_status(unsigned int *flags, bool clear);
@@ -134,6 +138,25 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
     return MLA_OK;
 }
 
+mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits, const void *w_uv,
+                                const void *gate, const int32_t *lengths, int num_requests, int qlen, int heads,
+                                void *out, void *latent, float *lse_out, void *stream) {
+    if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return fail(MLA_ERR_INVALID, "num_splits outside 1..256");
+    if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
+    if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
+    if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
+    if (num_requests == 0) return MLA_OK;
+    if (!o || !lse || !w_uv || !gate || !lengths || !out) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(o, 16) || !aligned(w_uv, 16) || !aligned(latent, 16) || !aligned(lse, 4) || !aligned(gate, 4) ||
+        !aligned(out, 4) || !aligned(lengths, 4) || !aligned(lse_out, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (o, w_uv, latent need 16 bytes)");
+    if ((int64_t)num_requests * qlen > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
+    cudaError_t e = mla::merge_value_launch(o, lse, num_splits, w_uv, gate, lengths, num_requests, qlen, heads, out,
+                                            latent, lse_out, device_sms(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge_value_gate launch");
+    return MLA_OK;
+}
+
 int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
                       const int32_t *host_lengths, int sm_count, int *split_tokens) {
     if (sm_count <= 0) sm_count = device_sms();
@@ -220,7 +243,7 @@ mla_status mla_device_status(void *stream, unsigned int *flags) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::attend_tc_status, mla::merge_status,
-                                                      mla::value_gate_status, mla::gather_status};
+                                                      mla::value_gate_status, mla::gather_status, mla::merge_value_status};
     for (auto rd : readers) {
         unsigned int f = 0;
         e = rd(&f, true);

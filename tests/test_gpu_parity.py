@@ -181,6 +181,36 @@ def test_value_gate_standalone(R, qlen, heads):
     assert torch.all(out[torch.from_numpy(dead).to(DEV)] == 0)
 
 
+@pytest.mark.parametrize("idx,lengths", SMALL)
+def test_fused_merge_value_matches_oracle_and_two_call_path(idx, lengths):
+    """mla_merge_value_gate against the oracle, and byte-equal to merge followed
+    by value_gate (same roundings, same order)."""
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 4, 40)
+    lat2 = torch.empty_like(latent)
+    lse2 = torch.empty_like(lse_m)
+    out2 = mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, inp.qlen, latent=lat2, lse_out=lse2)
+    torch.cuda.synchronize()
+    _check_full(lat2, lse2, out2, inp_cpu)
+    assert torch.equal(out2, out) and torch.equal(lat2, latent)
+    assert torch.equal(torch.nan_to_num(lse2, neginf=-1e30), torch.nan_to_num(lse_m, neginf=-1e30))
+
+
+@pytest.mark.parametrize("splits,R,qlen,heads", [(1, 3, 1, 12), (6, 70, 1, 12), (9, 40, 8, 12), (3, 2, 1, 96)])
+def test_fused_merge_value_standalone(splits, R, qlen, heads):
+    S = R * qlen
+    o, lse = W.make_partials(splits, S, heads, seed=R)
+    g = torch.Generator().manual_seed(R)
+    w = (torch.randn(heads, 128, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    gate = torch.randn(S, heads * 128, generator=g).to(torch.bfloat16)
+    lengths = torch.randint(0, 3, (R,), generator=g, dtype=torch.int32)
+    out = mla.merge_value_gate(o.to(DEV), lse.to(DEV), w.to(DEV), gate.to(DEV), lengths.to(DEV), qlen)
+    rl, _ = O.merge(O.bf16_to_f64(bf16_bits(o)), lse.double().numpy())
+    ref = O.value_gate(rl, bf16_bits(w), bf16_bits(gate), lengths.numpy(), qlen)
+    assert_bf16_close(out, ref, "fused merge+value")
+
+
 # ----------------------------------------------------------------- page gather
 
 @pytest.mark.parametrize("idx,lengths", SMALL)
