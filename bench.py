@@ -188,7 +188,7 @@ def run_gpu(args):
                 ev[2].record(stream)
             mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=stream)
         else:
-            mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=stream)
+            mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, latent=latent, stream=stream)
             if ev:
                 ev[2].record(stream)
         if ev:
@@ -242,7 +242,7 @@ def run_gpu(args):
             mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
             mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
         else:
-            mla.merge_value_gate(o, lse, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
+            mla.merge_value_gate(o, lse, inp.w_uv, gate_d, lens_d, qlen, out=out, latent=latent, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

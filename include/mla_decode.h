@@ -144,9 +144,11 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
 
 /*
  * mla_merge_value_gate -- mla_merge_splits followed by mla_value_gate in one
- * launch: the merged latent is formed in shared memory (rounded to bf16, as
- * the two-call path rounds it) and projected and gated without a round trip
- * through global memory.
+ * call.  Small batches (at most half as many 16-row tiles x heads as SMs)
+ * run as a single launch that forms the merged latent in shared memory and
+ * projects and gates it straight away; larger ones run the two kernels.
+ * Both routes give the same bytes as the two calls (the latent is rounded
+ * to bf16 before the projection).
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
  * m1c_inputs / post (the LSE merge of the splits, then W_UV and the gate)
@@ -155,8 +157,8 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
  *
  *   o, lse, num_splits   as mla_merge_splits (rows = num_requests * qlen)
  *   w_uv, gate, lengths  as mla_value_gate;  out bf16 [S, heads*128] (written)
- *   latent, lse_out      optional (may be NULL): the merged latent
- *                        bf16 [S, heads, 512] and LSE f32 [S, heads]
+ *   latent               bf16 [S, heads, 512] (written: the merged latent)
+ *   lse_out              f32 [S, heads] (written; may be NULL)
  */
 mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits, const void *w_uv,
                                 const void *gate, const int32_t *lengths, int num_requests, int qlen,

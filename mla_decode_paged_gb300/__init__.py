@@ -181,9 +181,9 @@ def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
 
 def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=None, lse_out=None,
                      stream=None):
-    """Merge + W_UV + gate in one launch: returns ``out [S, heads*128] bf16``.
-    ``latent`` / ``lse_out`` (optional tensors) also receive the merged
-    latent and LSE."""
+    """Merge + W_UV + gate in one call (one launch for small batches):
+    returns ``out [S, heads*128] bf16``.  ``latent`` (allocated if not given)
+    receives the merged latent, ``lse_out`` (optional) the merged LSE."""
     _need(o.dtype == torch.bfloat16 and o.dim() == 4 and o.shape[3] == D_LATENT and o.is_contiguous(),
           "o must be contiguous bf16 [splits, S, heads, 512]")
     _need(lse.dtype == torch.float32 and lse.shape == o.shape[:3] and lse.is_contiguous(),
@@ -202,6 +202,8 @@ def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=No
               "lse_out must be contiguous f32 [S, heads]")
     if out is None:
         out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=o.device)
+    if latent is None:
+        latent = torch.empty((S, H, D_LATENT), dtype=torch.bfloat16, device=o.device)
     st = library().mla_merge_value_gate(_ptr(o), _ptr(lse), ns, _ptr(w_uv), _ptr(gate), _ptr(lengths),
                                         lengths.numel(), qlen, H, _ptr(out), _ptr(latent), _ptr(lse_out),
                                         ctypes.c_void_p(_stream(stream)))

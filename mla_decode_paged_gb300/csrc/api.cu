@@ -146,13 +146,25 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
     if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
     if (num_requests == 0) return MLA_OK;
-    if (!o || !lse || !w_uv || !gate || !lengths || !out) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!o || !lse || !w_uv || !gate || !lengths || !out || !latent) return fail(MLA_ERR_INVALID, "null pointer");
     if (!aligned(o, 16) || !aligned(w_uv, 16) || !aligned(latent, 16) || !aligned(lse, 4) || !aligned(gate, 4) ||
         !aligned(out, 4) || !aligned(lengths, 4) || !aligned(lse_out, 4))
         return fail(MLA_ERR_INVALID, "misaligned pointer (o, w_uv, latent need 16 bytes)");
     if ((int64_t)num_requests * qlen > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
-    cudaError_t e = mla::merge_value_launch(o, lse, num_splits, w_uv, gate, lengths, num_requests, qlen, heads, out,
-                                            latent, lse_out, device_sms(), static_cast<cudaStream_t>(stream));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int sms = device_sms();
+    const int64_t S = (int64_t)num_requests * qlen;
+    cudaError_t e;
+    if (((S + 15) / 16) * heads <= sms / 2) {
+        e = mla::merge_value_launch(o, lse, num_splits, w_uv, gate, lengths, num_requests, qlen, heads, out, latent,
+                                    lse_out, sms, st);
+    } else {
+        // Larger batches: a fused kernel would re-read every partial row
+        // once per column block; the two kernels read each once.
+        e = mla::merge_launch(o, lse, num_splits, (int)S, heads, latent, lse_out, st);
+        if (e == cudaSuccess)
+            e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "merge_value_gate launch");
     return MLA_OK;
 }

@@ -10,13 +10,14 @@
 // mla_merge_splits followed by mla_value_gate (the merged latent is rounded
 // to bf16 before the projection), in one launch.
 //
-// Design: one CTA (4 warps) per (16 rows, head, COLS output columns).  One
-// warp bulk-copies the CTA's W_UV rows into padded smem while every warp
-// LSE-merges 4 latent rows straight into smem (lanes own 16 columns, split
+// Design: one CTA (16 warps) per (16 rows, head, COLS output columns).
+// One warp bulk-copies the CTA's W_UV rows into padded smem while each warp
+// LSE-merges one latent row straight into smem (lanes own 16 columns, split
 // weights held one per lane, four splits' loads in flight); then warp MMA
-// (bf16, m16n8k16) over the 512-wide latent and the gate epilogue.  Small
-// batches use COLS = 32 (four CTAs per row tile, more SMs busy); large
-// ones COLS = 128 (each partial row read once).
+// (bf16, m16n8k16, one 8-column tile per warp) over the 512-wide latent and
+// the gate epilogue.  COLS = 32: four CTAs per row tile, so a small batch
+// still spreads over the SMs (the host routes large batches to the
+// separate merge and value kernels, which read each partial row once).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -25,7 +26,8 @@ namespace mla {
 namespace {
 
 constexpr int kRows = 16, kStride = MLA_D_LATENT + 8;  // bf16 elements per padded smem row
-constexpr int kThreads = 128;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
 
 template <int COLS>
 struct Smem {
@@ -113,12 +115,12 @@ __device__ void merge_row(const __nv_bfloat16 *__restrict__ o, const float *__re
 }
 
 template <int COLS>
-__global__ void __launch_bounds__(kThreads) merge_value_kernel(
+__global__ void __launch_bounds__(kThreads, 1) merge_value_kernel(
     const __nv_bfloat16 *__restrict__ o, const float *__restrict__ lse, int num_splits,
     const __nv_bfloat16 *__restrict__ w_uv, const __nv_bfloat16 *__restrict__ gate,
     const int32_t *__restrict__ lengths, int S, int qlen, int H, __nv_bfloat16 *__restrict__ out,
     __nv_bfloat16 *__restrict__ latent, float *__restrict__ lse_out) {
-    constexpr int NT = COLS / 32;   // 8-column MMA tiles per warp
+    constexpr int MW = COLS / 8;    // warps with an 8-column MMA tile
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<COLS> &sm = *reinterpret_cast<Smem<COLS> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -138,55 +140,40 @@ __global__ void __launch_bounds__(kThreads) merge_value_kernel(
             bulk_g2s(sm.w[i], w_uv + ((long long)h * MLA_D_V + v0 + i) * MLA_D_LATENT, MLA_D_LATENT * 2, &sm.bar);
     }
     // Gate words and row activity for the epilogue, in flight during the merge.
-    uint32_t gw[2][NT];
-    bool active[2];
+    uint32_t gw[2] = {0u, 0u};
+    bool active[2] = {false, false};
+    if (warp < MW) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int t = t0 + 8 * hh + g;
-        active[hh] = t < S && __ldg(lengths + t / qlen) > 0;
-        const long long rowoff = (long long)t * H * MLA_D_V + (long long)h * MLA_D_V + v0;
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-            gw[hh][n] = active[hh] ? __ldg(reinterpret_cast<const uint32_t *>(gate + rowoff + 8 * (warp * NT + n) + 2 * qd)) : 0u;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = t0 + 8 * hh + g;
+            active[hh] = t < S && __ldg(lengths + t / qlen) > 0;
+            const long long rowoff = (long long)t * H * MLA_D_V + (long long)h * MLA_D_V + v0;
+            if (active[hh]) gw[hh] = __ldg(reinterpret_cast<const uint32_t *>(gate + rowoff + 8 * warp + 2 * qd));
+        }
     }
-    // Merge 4 rows per warp into smem.
-    const long long nrow = (long long)S * H;
-#pragma unroll 1
-    for (int rr = 0; rr < 4; ++rr) {
-        const int r = warp * 4 + rr, t = t0 + r;
+    // One latent row per warp into smem.
+    {
+        const long long nrow = (long long)S * H;
+        const int t = t0 + warp;
         if (t < S) {
-            merge_row(o, lse, num_splits, nrow, (long long)t * H + h, sm.lat[r], writer ? latent : nullptr,
+            merge_row(o, lse, num_splits, nrow, (long long)t * H + h, sm.lat[warp], writer ? latent : nullptr,
                       writer ? lse_out : nullptr, lane);
         } else {
-            reinterpret_cast<uint4 *>(sm.lat[r])[lane] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4 *>(sm.lat[r])[32 + lane] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.lat[warp])[lane] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.lat[warp])[32 + lane] = make_uint4(0, 0, 0, 0);
         }
     }
     __syncthreads();
+    if (warp >= MW) return;
     if (!mbar_wait(&sm.bar, 0)) return;
 
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-#pragma unroll 4
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int ks = 0; ks < MLA_D_LATENT / 16; ++ks) {
-        uint32_t a[4];
+        uint32_t a[4], b0, b1;
         ldmatrix_x4(a, &sm.lat[lane & 15][16 * ks + (lane >> 4) * 8]);
-        if constexpr (NT == 1) {
-            uint32_t b0, b1;
-            ldmatrix_x2(b0, b1, &sm.w[8 * warp + (lane & 7)][16 * ks + ((lane >> 3) & 1) * 8]);
-            mma_bf16(acc[0], a, b0, b1);
-        } else {
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t b[4];
-                ldmatrix_x4(b, &sm.w[8 * (warp * NT + 2 * np) + (lane & 7) + ((lane >> 4) << 3)][16 * ks + ((lane >> 3) & 1) * 8]);
-                mma_bf16(acc[2 * np], a, b[0], b[1]);
-                mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-            }
-        }
+        ldmatrix_x2(b0, b1, &sm.w[8 * warp + (lane & 7)][16 * ks + ((lane >> 3) & 1) * 8]);
+        mma_bf16(acc, a, b0, b1);
     }
     // Epilogue: bf16(value) * sigmoid(gate) -> bf16; empty requests -> 0.
 #pragma unroll
@@ -194,16 +181,13 @@ __global__ void __launch_bounds__(kThreads) merge_value_kernel(
         const int t = t0 + 8 * hh + g;
         if (t >= S) continue;
         const long long rowoff = (long long)t * H * MLA_D_V + (long long)h * MLA_D_V + v0;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            uint32_t res = 0u;
-            if (active[hh]) {
-                const float v_lo = __bfloat162float(__float2bfloat16_rn(acc[n][2 * hh]));
-                const float v_hi = __bfloat162float(__float2bfloat16_rn(acc[n][2 * hh + 1]));
-                res = pack_bf16x2(v_lo * sigmoid_f32(bf16_lo(gw[hh][n])), v_hi * sigmoid_f32(bf16_hi(gw[hh][n])));
-            }
-            *reinterpret_cast<uint32_t *>(out + rowoff + 8 * (warp * NT + n) + 2 * qd) = res;
+        uint32_t res = 0u;
+        if (active[hh]) {
+            const float v_lo = __bfloat162float(__float2bfloat16_rn(acc[2 * hh]));
+            const float v_hi = __bfloat162float(__float2bfloat16_rn(acc[2 * hh + 1]));
+            res = pack_bf16x2(v_lo * sigmoid_f32(bf16_lo(gw[hh])), v_hi * sigmoid_f32(bf16_hi(gw[hh])));
         }
+        *reinterpret_cast<uint32_t *>(out + rowoff + 8 * warp + 2 * qd) = res;
     }
 }
 
@@ -229,12 +213,8 @@ cudaError_t merge_value_launch(const void *o, const float *lse, int num_splits, 
                                float *lse_out, int sms, cudaStream_t st) {
     const int S = R * qlen;
     if (S == 0) return cudaSuccess;
-    const long long tiles = (long long)((S + kRows - 1) / kRows) * H;
-    // Few row tiles: spread the 128 output columns over four CTAs (the
-    // partial rows are re-read from L2); many: one CTA per row tile.
-    if (tiles < 2LL * sms)
-        return launch<32>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
-    return launch<128>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
+    (void)sms;
+    return launch<32>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
 }
 
 cudaError_t merge_value_status(unsigned int *flags, bool clear) { return read_status(flags, clear); }

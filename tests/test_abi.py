@@ -87,7 +87,8 @@ def test_merge_and_value_gate_reject_bad_arguments(lib):
     assert lib.mla_value_gate(P16, NULL, P16, P16, 2, 1, 12, P16, NULL) == mla.MLA_ERR_INVALID
     assert lib.mla_debug_gather(P16, 10, P16, 5, P16, 1, 6, P16, NULL) == mla.MLA_ERR_INVALID
     assert lib.mla_merge_value_gate(P16, P16, 0, P16, P16, P16, 2, 1, 12, P16, NULL, NULL, NULL) == mla.MLA_ERR_INVALID
-    assert lib.mla_merge_value_gate(P16, P16, 2, NULL, P16, P16, 2, 1, 12, P16, NULL, NULL, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_merge_value_gate(P16, P16, 2, NULL, P16, P16, 2, 1, 12, P16, P16, NULL, NULL) == mla.MLA_ERR_INVALID
+    assert lib.mla_merge_value_gate(P16, P16, 2, P16, P16, P16, 2, 1, 12, P16, NULL, NULL, NULL) == mla.MLA_ERR_INVALID
     # empty work is a no-op, not an error (and launches nothing)
     assert lib.mla_merge_splits(P16, P16, 2, 0, 12, P16, NULL, NULL) == mla.MLA_OK
     assert lib.mla_value_gate(P16, P16, P16, P16, 0, 1, 12, P16, NULL) == mla.MLA_OK

@@ -197,8 +197,10 @@ def test_fused_merge_value_matches_oracle_and_two_call_path(idx, lengths):
     assert torch.equal(torch.nan_to_num(lse2, neginf=-1e30), torch.nan_to_num(lse_m, neginf=-1e30))
 
 
-@pytest.mark.parametrize("splits,R,qlen,heads", [(1, 3, 1, 12), (6, 70, 1, 12), (9, 40, 8, 12), (3, 2, 1, 96)])
+@pytest.mark.parametrize("splits,R,qlen,heads", [(1, 3, 1, 12), (6, 70, 1, 12), (9, 40, 8, 12), (3, 2, 1, 96),
+                                                 (5, 200, 8, 12)])
 def test_fused_merge_value_standalone(splits, R, qlen, heads):
+    """Both routes: one launch (small batches) and merge + value (large)."""
     S = R * qlen
     o, lse = W.make_partials(splits, S, heads, seed=R)
     g = torch.Generator().manual_seed(R)
