@@ -105,7 +105,7 @@ def _plan_stats(inp, ns, st):
 class Clocks:
     """nvidia-smi sampler running while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -119,12 +119,19 @@ class Clocks:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
         self.t0 = time.time()
+
+    def mark(self, begin):
+        """Wall-clock bounds of the timed region (samples outside are dropped)."""
+        if begin:
+            self.r0 = time.time()
+        else:
+            self.r1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -133,23 +140,29 @@ class Clocks:
         self.proc.terminate()
         self.proc.wait()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        import datetime
+        sm, mx, reasons, total = [], [], set(), 0
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        r0, r1 = getattr(self, "r0", 0.0), getattr(self, "r1", 1e30)
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names[1:], parts[5:9]):
+            total += 1
+            if not (r0 - 0.05 <= ts <= r1 + 0.05):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names[1:], parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
-        busy = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples_in_region": len(sm), "samples": total}
 
 
 def run_gpu(args):
@@ -208,10 +221,12 @@ def run_gpu(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark(True)
     for k in range(args.steps):
         flush.fill_(1.0)
         step(evs[k])
     torch.cuda.synchronize(dev)
+    clocks.mark(False)
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -335,7 +350,7 @@ def _ncu_traffic(workload):
     return int(vals["dram_bytes_per_launch"])
 
 
-def cpu_baseline(spec, inp, budget_s=15.0):
+def cpu_baseline(spec, inp, budget_s=10.0):
     """Time the plain C fp64 oracle on the host cores on a bounded sample of
     the workload's requests (the first requests until ~budget_s of work)."""
     import oracle  # test infrastructure: timed here as the CPU baseline only
@@ -359,13 +374,17 @@ def cpu_baseline(spec, inp, budget_s=15.0):
     while n > 1 and per_token * lens[:n].sum() / max(1, min(threads, n)) > budget_s:
         n = max(1, n // 2)
     reqs = list(range(n))
-    t0 = time.perf_counter()
-    oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
-                         requests=reqs)
-    dt = time.perf_counter() - t0
-    return {"value": n * spec.qlen / dt, "unit": UNIT, "cores": int(threads), "kind": "oracle",
-            "sample": "%d of %d requests (%d KV tokens), full path in fp64 C, %.2f s" % (
-                n, R, int(lens[:n].sum()), dt)}
+    reps, t0 = 0, time.perf_counter()
+    while True:   # repeat the sample until about the budget has been spent
+        oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
+                             requests=reqs)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or dt / reps * (reps + 1) > 2 * budget_s:
+            break
+    return {"value": n * spec.qlen * reps / dt, "unit": UNIT, "cores": int(threads), "kind": "oracle",
+            "sample": "%d of %d requests (%d KV tokens) x %d repetitions, full path in fp64 C, %.2f s" % (
+                n, R, int(lens[:n].sum()), reps, dt)}
 
 
 def run_reference(args):
@@ -399,7 +418,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=W.WORKLOADS[1].name)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
