@@ -82,6 +82,8 @@ struct Misc {
     uint64_t s_full, p_full, q_ready, o_done, fin;
     uint32_t tmem;
     int abort_flag;
+    int first[4];           // this CTA's first tile: r, ntok, flags (published before any load)
+    uint64_t first_ready;
     float c[NQ];            // per query row: scale*kv_scale*log2(e) / 2^e (0 for padding rows)
     float m[NQ];            // reference max of the row, log2 domain
     float alpha[NQ];
@@ -168,6 +170,12 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
         }
     };
     Tile cur = iter.next(lane);
+    if (pw == 0 && lane == 0) {
+        ms.first[0] = cur.r;
+        ms.first[1] = cur.ntok;
+        ms.first[2] = cur.valid ? cur.flags : kMetaDone;
+        mbar_arrive(&ms.first_ready);
+    }
     int rows[4];
     fetch(cur, rows);
     int n_issued = 0;
@@ -237,9 +245,9 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
         const TileMeta M = ms.meta[s];
         if (M.flags & kMetaDone) break;
         if (M.ntok == 0) {
-            // Empty request: nothing to multiply; release the stage once the
-            // softmax has read its descriptor.
-            if (!(ok = wait_or_abort(&ms.p_full, (n_p++) & 1, &ms.abort_flag))) break;
+            // Empty request: nothing to multiply (the softmax warps read the
+            // descriptor on their own).
+            __syncwarp();
             if (lane == 0) mbar_arrive(&ms.kv_empty[s]);
             continue;
         }
@@ -398,16 +406,19 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
     float l[H2], cr[H2], c16[H2], mr[H2];
     int n_s = 0, n_units = 0;
     uint8_t *prow = sm + C::OffP + (t >> 3) * 1024 + (t & 7) * 128;
+    // The first unit's query is prepared while its first tile is loading;
+    // later ones at the end of the unit before them.
+    if (!wait_or_abort(&ms.first_ready, 0, &ms.abort_flag)) return;
+    if (!(ms.first[2] & kMetaDone) && ms.first[1] > 0) prep_query<NQ>(P, sm, ms.first[0], ms.first[2] >> 8);
     for (int it = 0;; ++it) {
         const int s = it % kStages;
         if (!wait_or_abort(&ms.kv_full[s], (it / kStages) & 1, &ms.abort_flag)) return;
         const TileMeta M = ms.meta[s];
+        __syncwarp();
         if (M.flags & kMetaDone) return;
+        if (lane == 0) mbar_arrive(&ms.kv_empty[s]);   // descriptor read
         const int grp = M.flags >> 8;
         const bool first = M.flags & kTileFirst, last = M.flags & kTileLast;
-        // The very first unit's query: prepared here; later ones at the end
-        // of the unit before them.
-        if (it == 0 && M.ntok > 0) prep_query<NQ>(P, sm, M.r, grp);
         const bool next_unit = (M.nxt_flags & kNxtValid) && M.nxt_ntok > 0 && last;
         if (M.ntok == 0) {
             // Empty request: LSE -inf for its rows and every split.
@@ -418,8 +429,6 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
                     P.lse[((int64_t)k * S + tt) * P.heads + rho % P.heads] = -INFINITY;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.p_full);   // descriptor read: the stage may be released
             if (next_unit) prep_query<NQ>(P, sm, M.nxt_r, M.nxt_flags >> 8);
             continue;
         }
@@ -597,13 +606,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ms.kv_full[s], kProdWarps);
-            mbar_init(&ms.kv_empty[s], 1);
+            // released by the softmax warps' read of the descriptor and the MMA warp
+            mbar_init(&ms.kv_empty[s], kSoftWarps + 1);
         }
         mbar_init(&ms.s_full, 1);
         mbar_init(&ms.p_full, kSoftWarps);
         mbar_init(&ms.q_ready, kSoftWarps);
         mbar_init(&ms.o_done, 1);
         mbar_init(&ms.fin, 1);
+        mbar_init(&ms.first_ready, 1);
         ms.abort_flag = 0;
         mbar_fence_init();
     }
