@@ -145,6 +145,50 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const float (&v)[N]) {
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Sums over the warp's 32 lanes of each of a lane's C values, by a
+// transposing butterfly: while C is even, a step exchanges half of the
+// values with the partner lane and keeps the sums of the other half, so
+// later steps move fewer values.  On return a lane holds colsum_count(C)
+// sums, of columns base + [0, count); lanes that differ only in the bits
+// colsum_dup(C) hold the same sums.
+__host__ __device__ constexpr int colsum_count(int c) {
+    for (int d = 16; d >= 1; d >>= 1)
+        if (c % 2 == 0) c /= 2;
+    return c;
+}
+__host__ __device__ constexpr int colsum_dup(int c) {
+    int m = 0;
+    for (int d = 16; d >= 1; d >>= 1) {
+        if (c % 2 == 0) c /= 2;
+        else m |= d;
+    }
+    return m;
+}
+template <int C, int D>
+__device__ __forceinline__ void colsum(float *v, int lane, int &base) {
+    if constexpr (D >= 1) {
+        if constexpr (C % 2 == 0) {
+            const bool up = (lane & D) != 0;
+#pragma unroll
+            for (int i = 0; i < C / 2; ++i) {
+                const float send = up ? v[i] : v[C / 2 + i];
+                const float keep = up ? v[C / 2 + i] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, D);
+            }
+            if (up) base += C / 2;
+            colsum<C / 2, D / 2>(v, lane, base);
+        } else {
+#pragma unroll
+            for (int i = 0; i < C; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], D);
+            colsum<C, D / 2>(v, lane, base);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ producers
 
 template <int NQ>
@@ -179,10 +223,23 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
     int rows[4];
     fetch(cur, rows);
     int n_issued = 0;
+    const int rows_total = P.qlen * P.heads;
     for (int it = 0; cur.valid; ++it) {
         Tile nxt = iter.next(lane);
         int nrows[4];
         fetch(nxt, nrows);
+        // The next unit's query rows into L2 (the softmax converts them when
+        // this unit ends).
+        if (pw == kProdWarps - 1 && nxt.valid && (nxt.flags & kTileFirst) && nxt.ntok > 0) {
+            const int grp = nxt.flags >> 8;
+            for (int i = lane; i < NQ * 9; i += 32) {
+                const int n = i / 9, line = i - 9 * n, rho = grp * NQ + n;
+                if (rho < rows_total) {
+                    const int tq = rho / P.heads, h = rho - tq * P.heads;
+                    prefetch_l2(P.q + ((int64_t)nxt.r * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK + 64 * line);
+                }
+            }
+        }
         const int s = it % kStages;
         if (!wait_or_abort(&ms.kv_empty[s], ((it / kStages) & 1) ^ 1, &ms.abort_flag)) return;
         const bool issue = has_op && cur.ntok > 0;
@@ -305,13 +362,13 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_total = P.qlen * P.heads;
-    constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6
-#pragma unroll 1
-    for (int i0 = 0; i0 < kPerWarp; i0 += 2) {
-        uint4 v[2][3];
-        bool valid[2];
+    constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6 rows per warp, all loads in flight at once
+    {
+        constexpr int i0 = 0;
+        uint4 v[kPerWarp][3];
+        bool valid[kPerWarp];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kPerWarp; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             const int rho = grp * NQ + n;
             valid[i] = rho < rows_total;
@@ -328,7 +385,7 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
             }
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kPerWarp; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             float amax = 0.f;
 #pragma unroll
@@ -549,14 +606,16 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
             // once this tile's P.V has been issued).
             if (next_unit) prep_query<NQ>(P, sm, M.nxt_r, M.nxt_flags >> 8);
             // ---- unit epilogue: row sums, o, lse
+            {
+                int cb = 0;
+                colsum<H2, 16>(l, lane, cb);
+                if ((lane & colsum_dup(H2)) == 0) {
 #pragma unroll
-            for (int j = 0; j < H2; ++j) {
-                float v = l[j];
+                    for (int i = 0; i < colsum_count(H2); ++i) ms.red[wq][n0 + cb + i] = l[i];
+                }
+                if (lane == 0 && wq == 0) {
 #pragma unroll
-                for (int dd = 16; dd; dd >>= 1) v += __shfl_xor_sync(0xffffffffu, v, dd);
-                if (lane == 0) {
-                    ms.red[wq][n0 + j] = v;
-                    if (wq == 0) ms.m[n0 + j] = mr[j];
+                    for (int j = 0; j < H2; ++j) ms.m[n0 + j] = mr[j];
                 }
             }
             if (!wait_or_abort(&ms.o_done, n_units & 1, &ms.abort_flag)) return;
@@ -575,22 +634,36 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
                 }
             }
             named_sync(kSoftBar, kSoftThreads);
-#pragma unroll 1
-            for (int b = 0; b < 4; ++b) {
-                float hi[H2], lo[H2];
-                ld_cols<H2>(tm + C::NP * (1 + b) + n0, hi);
-                ld_cols<H2>(tm + C::NP * (1 + b) + NQ + n0, lo);
-                tc::wait_ld();
+            // o rows: each latent block as bf16 [row][128] in the P' buffer
+            // (idle: this tile's P.V is done), then 16-byte row chunks out.
+            float iv[H2];
 #pragma unroll
-                for (int j = 0; j < H2; ++j) {
-                    const int64_t orow = ms.orow[n0 + j];
-                    if (orow >= 0)
-                        P.o[orow * MLA_D_LATENT + 128 * b + t] =
-                            __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * ms.invl[n0 + j]);
+            for (int j = 0; j < H2; ++j) iv[j] = ms.invl[n0 + j];
+            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + C::OffP);
+            constexpr int kBlkRound = 16384 / (NQ * 256);   // latent blocks staged at a time
+#pragma unroll 1
+            for (int b0 = 0; b0 < 4; b0 += kBlkRound) {
+#pragma unroll 1
+                for (int bb = 0; bb < kBlkRound; ++bb) {
+                    float hi[H2], lo[H2];
+                    ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + n0, hi);
+                    ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + NQ + n0, lo);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < H2; ++j)
+                        stg[(bb * NQ + n0 + j) * 128 + t] = __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * iv[j]);
                 }
+                named_sync(kSoftBar, kSoftThreads);
+                for (int c = tid; c < kBlkRound * NQ * 16; c += kSoftThreads) {
+                    const int row = c >> 4, ch = c & 15, bb = row / NQ, n = row - bb * NQ;
+                    const int64_t orow = ms.orow[n];
+                    if (orow >= 0)
+                        *reinterpret_cast<uint4 *>(P.o + orow * MLA_D_LATENT + 128 * (b0 + bb) + 8 * ch) =
+                            *reinterpret_cast<const uint4 *>(stg + row * 128 + 8 * ch);
+                }
+                named_sync(kSoftBar, kSoftThreads);
             }
             tc::fence_before();
-            named_sync(kSoftBar, kSoftThreads);
             ++n_units;
         }
     }
