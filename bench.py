@@ -8,7 +8,9 @@ one batch of the workload (default: 64 single-token requests, 12 heads,
 context lengths uniform in [1024, 8192], fp8 KV), inputs resident in HBM.
 L2 is flushed (a 256 MB write) before every timed step; only the step is
 inside the CUDA events.  ``value`` is query rows (tokens) per second over
-all ranks; ``e2e`` repeats the step through the public API with the step's
+all ranks, the step's launches replayed from one captured CUDA graph;
+``kernels_us`` and the roofline come from a second, eager pass with an
+event around each launch.  ``e2e`` repeats the step through the public API with the step's
 inputs copied from pinned host memory and its output read back, inside
 the timed region.  ``roofline`` is the attend kernel's algorithmic HBM bytes
 per launch over its event-timed duration, against the measured copy
@@ -188,53 +190,71 @@ def run_gpu(args):
     out = torch.empty((S, H * 128), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step(ev=None):
+    def step(strm, ev=None):
         if ev:
-            ev[0].record(stream)
+            ev[0].record(strm)
         mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, stream=stream)
+                   o=o, lse=lse, stream=strm)
         if ev:
-            ev[1].record(stream)
+            ev[1].record(strm)
         if args.three_call:
-            mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
+            mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=strm)
             if ev:
-                ev[2].record(stream)
-            mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=stream)
+                ev[2].record(strm)
+            mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=strm)
         else:
-            mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, latent=latent, stream=stream)
+            mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, latent=latent, stream=strm)
             if ev:
-                ev[2].record(stream)
+                ev[2].record(strm)
         if ev:
-            ev[3].record(stream)
+            ev[3].record(strm)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        step()
+        step(stream)
     torch.cuda.synchronize(dev)
     flags = mla.device_status()
     if flags:
         raise SystemExit("device status flags after warm-up: %#x" % flags)
+    # The whole step as one CUDA graph (its launches replayed without host work).
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream(dev))
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        graph.replay()
+    torch.cuda.synchronize(dev)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = Clocks(local)
     clocks.start()
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.mark(True)
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush.fill_(1.0)
-        step(evs[k])
+        gev[k][0].record(stream)
+        graph.replay()
+        gev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    t_step = [e[0].elapsed_time(e[3]) * 1e-3 for e in evs]
+    t_step = [e[0].elapsed_time(e[1]) * 1e-3 for e in gev]
+    total = sum(t_step)
+    # Per-launch times (eager launches, an event pair around each).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(1.0)
+        step(stream, evs[k])
+    torch.cuda.synchronize(dev)
     t_att = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
     t_mrg = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
     t_val = [e[2].elapsed_time(e[3]) * 1e-3 for e in evs]
-    total = sum(t_step)
+    if mla.device_status():
+        raise SystemExit("device status flags after the timed steps")
 
     # ---- end to end through the public API with host buffers
     q_h = inp.q.cpu().pin_memory()
@@ -306,6 +326,7 @@ def run_gpu(args):
             "kv": "fp8-e4m3 paged (page size 1)",
             "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 mma.sync (W_UV)",
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
+            "timing": "value: CUDA-graph replay of the step; kernels_us / roofline: eager launches, one event pair each",
         },
         "kernels_us": ({"attend": att * 1e6, "merge": statistics.mean(t_mrg) * 1e6,
                         "value_gate": statistics.mean(t_val) * 1e6} if args.three_call else
