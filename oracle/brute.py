@@ -41,13 +41,15 @@ def bf16(bits: int) -> float:
 
 
 def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                w_uv_bits, gate_bits, dims=576, latent_dims=512, vdim=128):
+                w_uv_bits, gate_bits, dims=576, latent_dims=512, vdim=128, causal=False):
     """Nested loops over requests, rows, heads, tokens and dims.
 
     Inputs are nested Python sequences (or numpy arrays indexed one element
     at a time).  ``dims`` / ``latent_dims`` may be reduced for speed, the
-    formula is the same.  Returns ``(latent, lse, out)`` as nested lists:
-    latent[t][h][c], lse[t][h], out[t][h*vdim + v].
+    formula is the same.  With ``causal``, query row tq of a request with L
+    tokens only sees token positions j <= L - qlen + tq.  Returns
+    ``(latent, lse, out)`` as nested lists: latent[t][h][c], lse[t][h],
+    out[t][h*vdim + v].
     """
     R = len(indptr) - 1
     latent, lse_out, out = [], [], []
@@ -60,15 +62,19 @@ def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
         for tq in range(qlen):
             t = r * qlen + tq
             lat_t, lse_t, out_t = [], [], []
+            seen = rows
+            if causal:
+                last = len(rows) - qlen + tq          # last position this row may see
+                seen = [row for j, row in enumerate(rows) if j <= last]
             for h in range(heads):
                 qv = [bf16(int(q_bits[t][h][d])) for d in range(dims)]
                 scores = []
-                for row in rows:
+                for row in seen:
                     acc = 0.0
                     for d in range(dims):
                         acc += qv[d] * row[d]
                     scores.append(scale * acc)
-                if not rows:
+                if not seen:
                     lat = [0.0] * latent_dims
                     lse = -math.inf
                 else:
@@ -78,7 +84,7 @@ def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
                         ssum += math.exp(s - mx)
                     lse = mx + math.log(ssum)
                     lat = [0.0] * latent_dims
-                    for s, row in zip(scores, rows):
+                    for s, row in zip(scores, seen):
                         w = math.exp(s - lse)
                         for c in range(latent_dims):
                             lat[c] += w * row[c]

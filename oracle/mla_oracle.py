@@ -23,7 +23,10 @@ What the path computes, per request r, query row t (r*qlen <= t <
     out[t, h*128 + v] = val * sigmoid(gate[t, h*128 + v])  if L_r > 0 else 0
 
 Readings where the pages are silent (each one is listed with its reason in
-the design notes): no intra-request causal mask; natural-log LSE of the
+the design notes): no intra-request causal mask by default, and with
+``causal=True`` row tq of a request sees only its first L_r - qlen + tq + 1
+tokens (the speculative-decode convention: the request's last qlen tokens
+are its own query positions); natural-log LSE of the
 scaled scores; ``kv_scale`` multiplies the stored fp8 value and applies to
 both the score K and the value V; OCP e4m3fn; page size 1; the split plan
 of :func:`split_plan`; the gate is raw logits and the sigmoid is exact.
@@ -105,30 +108,49 @@ def gather_all(kv_codes, pages, indptr) -> np.ndarray:
 # Attention of one request
 # ---------------------------------------------------------------------------
 
-def attend_rows(q_rows, K, scale: float):
+def attend_rows(q_rows, K, scale: float, visible=None):
     """Softmax attention of query rows over one request's dequantised rows.
 
     ``q_rows``: float64 [n, 576] (n = qlen * H query rows of one request);
     ``K``: float64 [L, 576] (dequantised, kv_scale applied).  Multi-query
     form: every row attends over the same latent rows, keys are the full 576
     dims, values the first 512 (``attend``: forward_mqa on the latent cache).
+    ``visible``: optional per-row count of leading rows of K the row may see
+    (the causal mask); None means all L.
 
-    Returns ``(latent [n, 512], lse [n], p [n, L])``; for L == 0 the latent
-    is 0, the LSE -inf and p empty.
+    Returns ``(latent [n, 512], lse [n], p [n, L])``; a row that sees no
+    token gets latent 0, LSE -inf and p 0.
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
     n = q_rows.shape[0]
     L = K.shape[0]
+    vis = np.full(n, L, np.int64) if visible is None else np.clip(np.asarray(visible, np.int64), 0, L)
+    latent = np.zeros((n, D_LATENT))
+    lse = np.full(n, -np.inf)
+    p = np.zeros((n, L))
     if L == 0:
-        return np.zeros((n, D_LATENT)), np.full(n, -np.inf), np.zeros((n, 0))
+        return latent, lse, p
     s = scale * (q_rows @ K.T)                       # [n, L]
-    m = s.max(axis=1, keepdims=True)
-    e = np.exp(s - m)
-    denom = e.sum(axis=1, keepdims=True)
-    p = e / denom
-    lse = (m + np.log(denom))[:, 0]
-    latent = p @ K[:, :D_LATENT]
+    for i in range(n):
+        v = int(vis[i])
+        if v == 0:
+            continue
+        si = s[i, :v]
+        m = si.max()
+        e = np.exp(si - m)
+        denom = e.sum()
+        p[i, :v] = e / denom
+        lse[i] = m + np.log(denom)
+        latent[i] = p[i, :v] @ K[:v, :D_LATENT]
     return latent, lse, p
+
+
+def causal_visible(L: int, qlen: int, heads: int) -> np.ndarray:
+    """Per query row (order (tq, h), as the rows of :func:`attend_rows`), the
+    number of leading tokens it sees under the causal reading:
+    L - qlen + tq + 1, clipped to [0, L]."""
+    tq = np.repeat(np.arange(qlen, dtype=np.int64), heads)
+    return np.clip(int(L) - qlen + tq + 1, 0, int(L))
 
 
 def dequant(codes, kv_scale: float) -> np.ndarray:
@@ -138,13 +160,14 @@ def dequant(codes, kv_scale: float) -> np.ndarray:
 
 
 def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-           requests=None, return_p=False):
+           requests=None, return_p=False, causal=False):
     """The unsplit attention: latent [S, H, 512] and LSE [S, H].
 
     ``q_bits``: uint16 bf16 bits [S, H_pad, 576]; only heads < ``heads`` are
     read (``attend``: the real heads of a query padded 96 -> 128).
     ``requests``: optional subset of request indices to compute (others are
     left NaN), so that full-size workloads can be checked on a sample.
+    ``causal``: apply :func:`causal_visible` to each request's rows.
     """
     q = np.asarray(q_bits)
     R = len(indptr) - 1
@@ -155,7 +178,8 @@ def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     for r in (range(R) if requests is None else requests):
         K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
         rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
-        lat, l, p = attend_rows(rows, K, scale)
+        vis = causal_visible(K.shape[0], qlen, heads) if causal else None
+        lat, l, p = attend_rows(rows, K, scale, vis)
         latent[r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)
         lse[r * qlen:(r + 1) * qlen] = l.reshape(qlen, heads)
         ps[r] = p.reshape(qlen, heads, -1)
@@ -192,12 +216,14 @@ def split_plan(L: int, num_splits: int, split_tokens: int):
 
 
 def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                  num_splits, split_tokens, requests=None):
+                  num_splits, split_tokens, requests=None, causal=False):
     """Per-split partials: o [num_splits, S, H, 512] (float64) and lse
     [num_splits, S, H]; each used split is the attention restricted to its
     token range (``m1c_inputs``: new partials o [splits, S, 12, 512], LSE
     [splits, S, 12], merged afterwards).  Unused splits hold lse = -inf and
-    o = NaN (their o is unspecified)."""
+    o = NaN (their o is unspecified).  With ``causal``, a split's partial for
+    a row covers the tokens of the split's range that the row sees; a row
+    that sees none of them gets lse = -inf there."""
     q = np.asarray(q_bits)
     R = len(indptr) - 1
     S = R * qlen
@@ -209,8 +235,9 @@ def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
         lse[:, r * qlen:(r + 1) * qlen] = -np.inf
         K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
         rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
+        vis = causal_visible(K.shape[0], qlen, heads) if causal else np.full(qlen * heads, K.shape[0])
         for k, (a, b) in enumerate(split_plan(K.shape[0], num_splits, split_tokens)):
-            lat, l, _ = attend_rows(rows, K[a:b], scale)
+            lat, l, _ = attend_rows(rows, K[a:b], scale, vis - a)
             if b > a:
                 o[k, r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)
             lse[k, r * qlen:(r + 1) * qlen] = l.reshape(qlen, heads)
@@ -275,11 +302,11 @@ def value_gate(latent, w_uv_bits, gate_bits, lengths, qlen):
 
 
 def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                w_uv_bits, gate_bits, lengths, requests=None):
+                w_uv_bits, gate_bits, lengths, requests=None, causal=False):
     """The whole step from raw inputs: (latent, lse, out).  With
     ``requests``, only those requests' rows are filled (the rest NaN)."""
     latent, lse = attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                         requests=requests)
+                         requests=requests, causal=causal)
     lat_in = np.nan_to_num(latent, nan=0.0)
     out = value_gate(lat_in, w_uv_bits, gate_bits, lengths, qlen)
     if requests is not None:

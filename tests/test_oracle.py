@@ -325,3 +325,72 @@ def test_c_oracle_matches_numpy_oracle():
         f = np.isfinite(lse)
         assert np.allclose(clse[f], lse[f], atol=1e-12)
         assert np.allclose(cout, out, atol=1e-12, rtol=1e-12)
+
+
+# --------------------------------------------------------- causal reading
+
+def _spec_like(seed=3, R=3, qlen=4, H=2, lens=(2, 9, 40)):
+    """Small speculative-decode inputs (qlen > 1), including a request shorter than qlen."""
+    q, kv, pages, indptr, w, gate, lens = _random_tiny(seed, R=R, qlen=qlen, H=H, lens=lens)
+    return dict(q_bits=q, kv_codes=kv, pages=pages, indptr=indptr, scale=1 / math.sqrt(192), kv_scale=0.8,
+                heads=H, qlen=qlen), w, gate, lens
+
+
+def test_causal_single_row_equals_unmasked():
+    """With qlen 1 the causal reading shows every row all L_r tokens."""
+    inp = W.make_inputs(0)
+    a = oracle_args(inp)
+    lat, lse = O.attend(**a)
+    clat, clse = O.attend(**a, causal=True)
+    assert np.array_equal(lat, clat) and np.array_equal(lse, clse)
+
+
+def test_causal_row_equals_truncated_context():
+    """Row tq of a request under the mask equals the unmasked attention of a
+    request whose pages are cut to its first L - qlen + tq + 1 entries."""
+    a, _, _, _ = _spec_like()
+    qlen, H = a["qlen"], a["heads"]
+    clat, clse = O.attend(**a, causal=True)
+    R = len(a["indptr"]) - 1
+    for r in range(R):
+        lo, hi = int(a["indptr"][r]), int(a["indptr"][r + 1])
+        L = hi - lo
+        for tq in range(qlen):
+            keep = max(0, L - qlen + tq + 1)
+            t = r * qlen + tq
+            pages = np.asarray(a["pages"][lo:lo + keep], np.int32)
+            lat1, lse1 = O.attend(a["q_bits"][t:t + 1], a["kv_codes"], pages, np.array([0, keep], np.int32),
+                                  a["scale"], a["kv_scale"], H, 1)
+            assert np.allclose(clat[t], lat1[0], atol=1e-12, rtol=1e-12)
+            if keep == 0:
+                assert np.all(np.isneginf(clse[t])) and np.all(clat[t] == 0)
+            else:
+                assert np.allclose(clse[t], lse1[0], atol=1e-12)
+
+
+def test_causal_matches_brute_force():
+    a, w, gate, lens = _spec_like(seed=5)
+    lat, lse, out = O.decode_step(**a, w_uv_bits=w, gate_bits=gate, lengths=lens, causal=True)
+    blat, blse, bout = brute.decode_step(a["q_bits"], a["kv_codes"], a["pages"], a["indptr"], a["scale"],
+                                         a["kv_scale"], a["heads"], a["qlen"], w, gate, causal=True)
+    assert np.allclose(lat, np.array(blat), atol=1e-12, rtol=1e-12)
+    b = np.array(blse)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(b))
+    f = np.isfinite(b)
+    assert np.allclose(lse[f], b[f], atol=1e-12)
+    assert np.allclose(out, np.array(bout), atol=1e-12, rtol=1e-12)
+    # the mask actually changes the early rows of the long request
+    ulat, _ = O.attend(**a)
+    assert not np.allclose(ulat[2 * 4], lat[2 * 4])
+
+
+@pytest.mark.parametrize("ns,st", [(3, 4), (8, 5), (16, 1)])
+def test_causal_merge_of_splits_equals_unsplit(ns, st):
+    a, _, _, _ = _spec_like(seed=7)
+    lat, lse = O.attend(**a, causal=True)
+    o, ls = O.attend_splits(**a, num_splits=ns, split_tokens=st, causal=True)
+    mlat, mlse = O.merge(o, ls)
+    assert np.allclose(mlat, lat, atol=1e-12, rtol=1e-12)
+    assert np.array_equal(np.isneginf(mlse), np.isneginf(lse))
+    f = np.isfinite(lse)
+    assert np.allclose(mlse[f], lse[f], atol=1e-12)
