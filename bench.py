@@ -194,7 +194,7 @@ def run_gpu(args):
         if ev:
             ev[0].record(strm)
         mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, stream=strm)
+                   o=o, lse=lse, causal=args.causal, stream=strm)
         if ev:
             ev[1].record(strm)
         if args.three_call:
@@ -272,7 +272,7 @@ def run_gpu(args):
         for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h)):
             d.copy_(h, non_blocking=True)
         mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, stream=stream)
+                   o=o, lse=lse, causal=args.causal, stream=stream)
         if args.three_call:
             mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
             mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
@@ -324,6 +324,7 @@ def run_gpu(args):
             "l2": "flushed before every timed step (256 MB write, outside the events)",
             "parallelism": "replicas" if ws > 1 else "single-gpu",
             "kv": "fp8-e4m3 paged (page size 1)",
+            "mask": "causal within a request" if args.causal else "none",
             "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 mma.sync (W_UV)",
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
             "timing": "value: CUDA-graph replay of the step; kernels_us / roofline: eager launches, one event pair each",
@@ -447,6 +448,8 @@ def main():
     ap.add_argument("--three-call", action="store_true",
                     help="time merge and value/gate as two launches instead of the fused one")
     ap.add_argument("--ref-budget", type=float, default=5.0)
+    ap.add_argument("--causal", action="store_true",
+                    help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

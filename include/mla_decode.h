@@ -75,7 +75,8 @@ typedef int mla_status;
  *   s_j = scale * <q[t, h, :], K_j>
  *   lse[k, t, h] = ln sum_j exp(s_j)
  *   o[k, t, h, :] = sum_j exp(s_j - lse[k, t, h]) * K_j[:512]
- * No mask within a request: every row of r attends over all of r's tokens.
+ * No mask within a request: every row of r attends over all of r's tokens
+ * (mla_decode_attend_ex with MLA_ATTEND_CAUSAL adds the causal reading).
  *
  * Split plan: request r (length L_r = indptr[r+1] - indptr[r]) is cut into
  *   n_r = min(num_splits, max(1, ceil(L_r / split_tokens)))
@@ -102,6 +103,30 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
                              const int32_t *indptr, int num_requests, int qlen, int heads,
                              float scale, float kv_scale, int num_splits, int split_tokens,
                              void *o, float *lse, void *stream);
+
+/* Flags of mla_decode_attend_ex. */
+#define MLA_ATTEND_CAUSAL 1u   /* causal mask within a request (qlen > 1)    */
+
+/*
+ * mla_decode_attend_ex -- mla_decode_attend with option flags.
+ *
+ * The pages give no mask within a request; MLA_ATTEND_CAUSAL applies the
+ * speculative-decode reading (a request's qlen query rows are its last qlen
+ * token positions): row tq (0 <= tq < qlen) of request r sees only the
+ * first L_r - qlen + tq + 1 of r's tokens.  Each split's partial for a row
+ * covers the tokens of the split's range that the row sees; where it sees
+ * none, lse = -inf and o is 0 (so a row that sees no token at all merges
+ * to latent 0, LSE -inf).  flags = 0 is exactly mla_decode_attend.
+ *
+ * Arguments as mla_decode_attend.  Unknown flag bits: MLA_ERR_INVALID.
+ * MLA_ATTEND_CAUSAL with the warp-MMA kernel (environment
+ * MLA_ATTEND_KERNEL=mma): MLA_ERR_UNSUPPORTED.
+ */
+mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void *kv,
+                                int64_t pool_rows, const int32_t *pages, int64_t num_pages,
+                                const int32_t *indptr, int num_requests, int qlen, int heads,
+                                float scale, float kv_scale, int num_splits, int split_tokens,
+                                void *o, float *lse, unsigned int flags, void *stream);
 
 /*
  * mla_merge_splits -- LSE merge of split partials into the latent.

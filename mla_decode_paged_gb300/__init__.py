@@ -26,6 +26,7 @@ from . import build as _build
 
 D_QK, D_LATENT, D_V = 576, 512, 128
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
+ATTEND_CAUSAL = 1
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
 
 __all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "debug_gather",
@@ -62,13 +63,15 @@ def library() -> ctypes.CDLL:
     vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     lib.mla_decode_attend.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32,
                                       vp, vp, vp]
+    lib.mla_decode_attend_ex.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32,
+                                         vp, vp, ctypes.c_uint, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.mla_merge_value_gate.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
-    for name in ("mla_decode_attend", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
+    for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
                  "mla_device_status", "mla_choose_splits"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -114,13 +117,15 @@ def _as_u8(kv: torch.Tensor) -> torch.Tensor:
 
 
 def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
-           o=None, lse=None, stream=None):
+           o=None, lse=None, causal=False, stream=None):
     """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
     lse [num_splits, S, heads] f32)``.
 
     ``q``: bf16 ``[S, H_pad, 576]`` whose rows may be strided (a padded query:
     ``heads`` < H_pad reads only the first ``heads``); ``kv``: ``[pool, 576]``
     fp8 codes; ``pages``/``indptr``: int32; S = (len(indptr) - 1) * qlen.
+    ``causal``: row tq of a request sees only its first L - qlen + tq + 1
+    tokens (``mla_decode_attend_ex`` with ``MLA_ATTEND_CAUSAL``).
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
@@ -136,10 +141,10 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
         o = torch.empty((num_splits, S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((num_splits, S, heads), dtype=torch.float32, device=q.device)
-    st = library().mla_decode_attend(
+    st = library().mla_decode_attend_ex(
         _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr), R, qlen,
         heads, float(scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o), _ptr(lse),
-        ctypes.c_void_p(_stream(stream)))
+        ATTEND_CAUSAL if causal else 0, ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_decode_attend")
     return o, lse
 
@@ -250,17 +255,17 @@ def device_status(stream=None) -> int:
 
 
 def decode_step(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, *, heads=None, qlen=1,
-                num_splits=None, split_tokens=None, max_len=None, total_len=0, stream=None):
+                num_splits=None, split_tokens=None, max_len=None, total_len=0, causal=False, stream=None):
     """The whole step (attend -> merge -> value_gate); returns
     ``(out, latent, lse)``.  Without a split plan one is chosen from
-    ``max_len`` (host-known longest request)."""
+    ``max_len`` (host-known longest request).  ``causal`` as in :func:`attend`."""
     heads = q.shape[1] if heads is None else heads
     if num_splits is None or split_tokens is None:
         if max_len is None:
             raise ValueError("give num_splits and split_tokens, or max_len for the split plan")
         num_splits, split_tokens = choose_splits(indptr.numel() - 1, qlen, heads, max_len, total_len)
     o, lse = attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, heads=heads,
-                    qlen=qlen, stream=stream)
+                    qlen=qlen, causal=causal, stream=stream)
     latent, lse_m = merge(o, lse, stream=stream)
     out = value_gate(latent, w_uv, gate, lengths, qlen, stream=stream)
     return out, latent, lse_m

@@ -21,7 +21,7 @@ cudaError_t attend_mma_status(unsigned int *flags, bool clear);
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, int grid, cudaStream_t st);
+                             float *lse, bool causal, int grid, cudaStream_t st);
 cudaError_t attend_tc_status(unsigned int *flags, bool clear);
 cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
                          void *latent, float *lse_out, cudaStream_t st);
@@ -77,6 +77,17 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr,
                              int num_requests, int qlen, int heads, float scale, float kv_scale,
                              int num_splits, int split_tokens, void *o, float *lse, void *stream) {
+    return mla_decode_attend_ex(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, num_requests, qlen,
+                                heads, scale, kv_scale, num_splits, split_tokens, o, lse, 0u, stream);
+}
+
+mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                                int num_requests, int qlen, int heads, float scale, float kv_scale,
+                                int num_splits, int split_tokens, void *o, float *lse, unsigned int flags,
+                                void *stream) {
+    if (flags & ~MLA_ATTEND_CAUSAL) return fail(MLA_ERR_INVALID, "unknown flag bits");
+    const bool causal = (flags & MLA_ATTEND_CAUSAL) != 0;
     if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
     if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
     if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
@@ -94,6 +105,7 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
         return fail(MLA_ERR_INVALID, "misaligned pointer (q, kv, o need 16 bytes)");
     if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
     if (pool_rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "pool_rows above 2^31 - 1");
+    if (causal && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "causal mask with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_warp_mma()
                         ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
@@ -101,7 +113,7 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
                                                  split_tokens, o, lse, device_sms(), st)
                         : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                split_tokens, o, lse, device_sms(), st);
+                                                split_tokens, o, lse, causal, device_sms(), st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }

@@ -30,7 +30,8 @@
 //     reference max (rebased, and O rescaled in TMEM, only when a score
 //     exceeds it by more than 2^8), write P' (hi/lo e4m3) to smem, prepare
 //     the next unit's query, and at a unit's end reduce the row sums and
-//     write o / lse.
+//     write o / lse.  With the causal option, column n (query row tq) masks
+//     token positions >= L_r - qlen + tq + 1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
@@ -71,6 +72,7 @@ struct Cfg {
 struct TileMeta {
     int r, k, n_r, ntok, flags;         // flags: kTileFirst / kTileLast / kMetaDone, row group << 8
     int nxt_r, nxt_ntok, nxt_flags;     // nxt_flags = 0: no next tile
+    int tok0;                           // the tile's first token position in its request
 };
 constexpr int kMetaDone = 4, kNxtValid = 16;
 
@@ -84,6 +86,7 @@ struct Misc {
     int abort_flag;
     int first[4];           // this CTA's first tile: r, ntok, flags (published before any load)
     uint64_t first_ready;
+    int vis[NQ];            // causal: tokens of the request each query column sees
     float c[NQ];            // per query row: scale*kv_scale*log2(e) / 2^e (0 for padding rows)
     float m[NQ];            // reference max of the row, log2 domain
     float alpha[NQ];
@@ -98,7 +101,7 @@ struct Params {
     const int32_t *pages;
     int64_t num_pages;
     const int32_t *indptr;
-    int R, qlen, heads, num_splits, split_tokens, row_groups, nq;
+    int R, qlen, heads, num_splits, split_tokens, row_groups, nq, causal;
     float sc_log2;
     float kv_scale;
     __nv_bfloat16 *o;
@@ -251,6 +254,7 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
                 TileMeta m;
                 m.r = cur.r; m.k = cur.k; m.n_r = cur.n_r; m.ntok = cur.ntok; m.flags = cur.flags;
                 m.nxt_r = nxt.r; m.nxt_ntok = nxt.ntok; m.nxt_flags = nxt.valid ? (nxt.flags | kNxtValid) : 0;
+                m.tok0 = cur.tok0;
                 ms.meta[s] = m;
             }
             mbar_arrive_expect_tx(&ms.kv_full[s], bytes);
@@ -450,8 +454,9 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
 // tile (latent row t of O in the epilogue) and query columns
 // [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale), c/16 and
 // the reference max m in registers.  The tile sequence comes from the
-// stage descriptors.
-template <int NQ>
+// stage descriptors.  CAUSAL compiles the causal mask in (a separate
+// instantiation, so the unmasked path carries none of its work).
+template <int NQ, bool CAUSAL>
 __device__ void softmax(const Params &P, uint8_t *sm) {
     using C = Cfg<NQ>;
     constexpr int H2 = C::HALF;
@@ -503,7 +508,13 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
                 ms.orow[tid] = rho < rows_total
                                    ? ((int64_t)M.k * S + (int64_t)M.r * P.qlen + rho / P.heads) * P.heads + rho % P.heads
                                    : -1;
+                if (CAUSAL) {   // L_r from indptr (validated by the producers: ntok > 0 here)
+                    const int len = __ldg(P.indptr + M.r + 1) - __ldg(P.indptr + M.r);
+                    ms.vis[tid] = len - P.qlen + rho / P.heads + 1;
+                }
             }
+            // vis[] is read below by every softmax thread in this same tile
+            if (CAUSAL) named_sync(kSoftBar, kSoftThreads);
         }
         // ---- scores (log2 domain) of this thread's token and columns
         if (!wait_or_abort(&ms.s_full, n_s & 1, &ms.abort_flag)) return;
@@ -517,9 +528,11 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
             ld_cols<H2>(tm + NQ + n0, lo);
             tc::wait_ld();
             const bool live = t < M.ntok;
+            const int pos = M.tok0 + t;   // token position in the request
 #pragma unroll
             for (int j = 0; j < H2; ++j) {
-                sc[j] = live ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                const bool seen = CAUSAL ? live && pos < ms.vis[n0 + j] : live;
+                sc[j] = seen ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
                 over |= sc[j] - mr[j] > kRebase;   // also true for every live token while m = -inf
             }
         }
@@ -575,7 +588,9 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
             float hv[2], lv[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float pv = exp2f(sc[j + e] - mr[j + e]);
+                // masked entries give 0 even while the column's m is still -inf
+                // (without the mask every column sees each tile's live tokens)
+                const float pv = (!CAUSAL || sc[j + e] > -INFINITY) ? exp2f(sc[j + e] - mr[j + e]) : 0.f;
                 l[j + e] += pv;
                 hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
                 lv[e] = (pv - hv[e]) * 16.f;
@@ -623,7 +638,7 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
             named_sync(kSoftBar, kSoftThreads);
             if (tid < NQ) {
                 const float lt = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
-                ms.invl[tid] = P.kv_scale / lt;
+                ms.invl[tid] = lt > 0.f ? P.kv_scale / lt : 0.f;   // a row that saw no token: o = 0
                 const int64_t orow = ms.orow[tid];
                 if (orow >= 0) {
                     P.lse[orow] = (ms.m[tid] + __log2f(lt)) * 0.69314718055994531f;
@@ -669,7 +684,7 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
     }
 }
 
-template <int NQ>
+template <int NQ, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap mlat, const __grid_constant__ CUtensorMap mrope, const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -700,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 256 x 184 + 256 x 72 = 65536.
     if (warp < kSoftWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
-        softmax<NQ>(P, sm);
+        softmax<NQ, CAUSAL>(P, sm);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
         if (warp == kMmaWarp) mma_issuer<NQ>(P, sm);
@@ -729,13 +744,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+template <int NQ, bool CAUSAL>
+cudaError_t launch_as(const CUtensorMap &ml, const CUtensorMap &mr, const Params &P, int grid, cudaStream_t st) {
+    const size_t smem = smem_bytes<NQ>();
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NQ, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    attend_tc_kernel<NQ, CAUSAL><<<grid, kThreads, smem, st>>>(ml, mr, P);
+    return cudaGetLastError();
+}
+
 template <int NQ>
 cudaError_t launch(const CUtensorMap &ml, const CUtensorMap &mr, const Params &P, int grid, cudaStream_t st) {
-    const size_t smem = smem_bytes<NQ>();
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attend_tc_kernel<NQ><<<grid, kThreads, smem, st>>>(ml, mr, P);
-    return cudaGetLastError();
+    return P.causal ? launch_as<NQ, true>(ml, mr, P, grid, st) : launch_as<NQ, false>(ml, mr, P, grid, st);
 }
 
 }  // namespace
@@ -754,7 +775,7 @@ void attend_tc_shape(int rows, int *groups, int *nq) {
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, int grid, cudaStream_t st) {
+                             float *lse, bool causal, int grid, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap ml, mr;
@@ -781,6 +802,7 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
     P.heads = heads;
     P.num_splits = num_splits;
     P.split_tokens = split_tokens;
+    P.causal = causal ? 1 : 0;
     P.sc_log2 = scale * kv_scale * 1.4426950408889634f;
     P.kv_scale = kv_scale;
     P.o = static_cast<__nv_bfloat16 *>(o);

@@ -79,6 +79,32 @@ def test_attend_rejects_bad_arguments(lib, kw, msg):
     assert msg in lib.mla_last_error()
 
 
+def _attend_ex(lib, flags, **kw):
+    a = dict(q=P16, q_row_stride=12 * 576, kv=P16, pool_rows=100, pages=P16, num_pages=10, indptr=P16,
+             R=2, qlen=4, heads=12, scale=0.1, kv_scale=1.0, num_splits=4, split_tokens=16, o=P16, lse=P16,
+             stream=NULL)
+    a.update(kw)
+    return lib.mla_decode_attend_ex(a["q"], a["q_row_stride"], a["kv"], a["pool_rows"], a["pages"], a["num_pages"],
+                                    a["indptr"], a["R"], a["qlen"], a["heads"], a["scale"], a["kv_scale"],
+                                    a["num_splits"], a["split_tokens"], a["o"], a["lse"], flags, a["stream"])
+
+
+def test_attend_ex_rejects_unknown_flags_and_checks_like_attend(lib):
+    assert _attend_ex(lib, 2) == mla.MLA_ERR_INVALID
+    assert b"flag" in lib.mla_last_error()
+    assert _attend_ex(lib, 0x80000000) == mla.MLA_ERR_INVALID
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL, qlen=0) == mla.MLA_ERR_INVALID
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL, q=NULL) == mla.MLA_ERR_INVALID
+    # no requests: nothing to launch
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL, R=0) == mla.MLA_OK
+
+
+def test_causal_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
+    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL) == mla.MLA_ERR_UNSUPPORTED
+    assert b"causal" in lib.mla_last_error()
+
+
 def test_merge_and_value_gate_reject_bad_arguments(lib):
     assert lib.mla_merge_splits(P16, P16, 0, 4, 12, P16, NULL, NULL) == mla.MLA_ERR_INVALID
     assert lib.mla_merge_splits(P16, P16, 2, 4, 0, P16, NULL, NULL) == mla.MLA_ERR_INVALID

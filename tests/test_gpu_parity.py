@@ -280,3 +280,73 @@ def test_full_size_workloads_sampled(idx, kernel):
     assert torch.all(out[dead] == 0) and torch.all(torch.isneginf(lse_m[dead]))
     assert torch.isfinite(lse_m[~dead]).all()
     assert mla.device_status() == 0
+
+
+# ------------------------------------------------------------- causal option
+
+CAUSAL_SMALL = [
+    # (workload index, lengths): qlen 4 / 8, requests shorter than qlen, several tiles, a ragged tail
+    (2, [2, 3, 257, 700]),
+    (4, [0, 5, 7, 200, 333]),
+    (2, [130, 1, 4]),
+]
+
+
+@pytest.mark.parametrize("idx,lengths", CAUSAL_SMALL)
+@pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (8, 50), (3, 7)])
+def test_causal_small_workloads_match_oracle(idx, lengths, plan):
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    ns, st = plan
+    o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st,
+                        heads=inp.heads, qlen=inp.qlen, causal=True)
+    latent, lse_m = mla.merge(o, lse)
+    out = mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, inp.qlen)
+    torch.cuda.synchronize()
+    a = oracle_args(inp_cpu)
+    ro, rl = O.attend_splits(**a, num_splits=ns, split_tokens=st, causal=True)
+    assert_lse_close(lse, rl, "causal partial lse")
+    assert_bf16_close(o, ro, "causal partial o", mask=np.isfinite(rl))
+    # a split a row sees nothing of: o written as 0, not left unspecified
+    seen_none = np.isneginf(rl) & ~np.isnan(ro[..., 0])
+    if seen_none.any():
+        assert torch.all(o[torch.from_numpy(seen_none).to(DEV)] == 0)
+    rlat, rlse, rout = O.decode_step(**a, w_uv_bits=bf16_bits(inp_cpu.w_uv), gate_bits=bf16_bits(inp_cpu.gate),
+                                     lengths=i32(inp_cpu.lengths), causal=True)
+    assert_lse_close(lse_m, rlse, "causal merged lse")
+    assert_bf16_close(latent, rlat, "causal latent")
+    assert_bf16_close(out, rout, "causal out")
+    assert mla.device_status() == 0
+
+
+def test_causal_is_exactly_unmasked_at_qlen_1():
+    inp = _to(W.make_inputs(1, "cpu", lengths=[1, 17, 128, 129, 300]), DEV)
+    a = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 4, 64, heads=inp.heads)
+    b = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 4, 64, heads=inp.heads,
+                   causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1])
+    used = torch.isfinite(a[1])                 # o of unused splits is unspecified
+    assert torch.equal(a[0][used], b[0][used])
+
+
+@pytest.mark.parametrize("idx", [2, 4])
+def test_causal_full_size_sampled(idx):
+    inp = W.make_inputs(idx, DEV)
+    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
+    out, latent, lse_m = mla.decode_step(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, inp.w_uv,
+                                         inp.gate, inp.lengths, heads=inp.heads, qlen=inp.qlen, num_splits=ns,
+                                         split_tokens=st, causal=True)
+    torch.cuda.synchronize()
+    lens = i32(inp.lengths)
+    reqs = _sample_requests(lens, seed=idx + 10)
+    a = dict(q_bits=bf16_bits(inp.q), kv_codes=u8(inp.kv), pages=i32(inp.pages), indptr=i32(inp.indptr),
+             scale=inp.scale, kv_scale=inp.kv_scale, heads=inp.heads, qlen=inp.qlen)
+    rlat, rlse, rout = O.decode_step(**a, w_uv_bits=bf16_bits(inp.w_uv), gate_bits=bf16_bits(inp.gate),
+                                     lengths=lens, requests=reqs, causal=True)
+    rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
+    assert_lse_close(lse_m[rows], rlse[rows], "causal lse (sampled)")
+    assert_bf16_close(latent[rows], rlat[rows], "causal latent (sampled)")
+    assert_bf16_close(out[rows], rout[rows], "causal out (sampled)")
+    assert torch.isfinite(latent).all() and torch.isfinite(out).all()
+    assert mla.device_status() == 0
