@@ -315,3 +315,63 @@ def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
             keep[r * qlen:(r + 1) * qlen] = True
         out[~keep] = np.nan
     return latent, lse, out
+
+
+# ---------------------------------------------------------------------------
+# KV-cache append (the step that writes the cache the decode step reads)
+# ---------------------------------------------------------------------------
+
+_E4M3_POS = None
+
+
+def _e4m3_positive_table():
+    """The 127 non-negative finite E4M3 values (codes 0x00..0x7E), ascending."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3fn_to_f64(np.arange(0x7F, dtype=np.uint8))
+    return _E4M3_POS
+
+
+def f64_to_e4m3fn(x) -> np.ndarray:
+    """Encode float64 values as OCP E4M3 codes: round to the nearest
+    representable value, ties to the even code (mantissa LSB 0); finite
+    magnitudes above 448 and infinities saturate to +-448; NaN gives 0x7F.
+    The sign of -0.0 and of negative values is kept.  (The cache write of
+    the pages converts x / k_scale to fp8; the saturating conversion is this
+    library's reading, the one CUDA's ``satfinite`` conversion makes.)"""
+    x = np.asarray(x, dtype=np.float64)
+    table = _e4m3_positive_table()
+    a = np.abs(x)
+    sat = np.where(np.isnan(a), 0.0, np.minimum(a, 448.0))
+    hi = np.clip(np.searchsorted(table, sat, side="left"), 0, len(table) - 1)
+    lo = np.clip(hi - 1, 0, len(table) - 1)
+    d_hi = table[hi] - sat
+    d_lo = sat - table[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def kv_append(kv_codes, kv_c_bits, k_pe_bits, slots, k_scale: float) -> np.ndarray:
+    """The cache after writing new tokens (vLLM API page
+    ``vllm.models.kimi_k3.amd.specialized_decode.runtime.mla``, ``pre``:
+    ``do_kv_cache_update`` stores the 512-wide ``kv_c`` and the 64-wide
+    ``k_pe`` of each token, divided by ``k_scale`` and converted to fp8, at
+    the token's slot of the flat token rows).
+
+    ``kv_codes``: uint8 [pool, 576] (not modified; a copy is returned);
+    ``kv_c_bits``: bf16 bits [T, 512]; ``k_pe_bits``: bf16 bits [T, 64];
+    ``slots``: int64 [T], a negative slot skips its token (padding).  The
+    quotient is taken in float32 (the precision the cache write computes
+    in), then encoded by :func:`f64_to_e4m3fn`.
+    """
+    out = np.array(kv_codes, dtype=np.uint8, copy=True)
+    rows = np.concatenate([bf16_to_f64(kv_c_bits), bf16_to_f64(k_pe_bits)], axis=1).astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        q = (rows / np.float32(k_scale)).astype(np.float64)
+    codes = f64_to_e4m3fn(q)
+    for i, s in enumerate(np.asarray(slots, np.int64)):
+        if s >= 0:
+            out[s] = codes[i]
+    return out

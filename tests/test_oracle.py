@@ -394,3 +394,52 @@ def test_causal_merge_of_splits_equals_unsplit(ns, st):
     assert np.array_equal(np.isneginf(mlse), np.isneginf(lse))
     f = np.isfinite(lse)
     assert np.allclose(mlse[f], lse[f], atol=1e-12)
+
+
+# ----------------------------------------------------- e4m3 encoder, KV append
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = O.e4m3fn_to_f64(codes)
+    assert np.array_equal(O.f64_to_e4m3fn(vals), codes)
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    g = torch.Generator().manual_seed(3)
+    x = torch.cat([torch.randn(20000, generator=g) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = x[x.abs() <= 448]
+    # every midpoint between adjacent representable values (ties to even)
+    t = torch.from_numpy(O.e4m3fn_to_f64(np.arange(0x7F, dtype=np.uint8)))
+    mids = ((t[1:] + t[:-1]) / 2).float()
+    x = torch.cat([x, mids, -mids, torch.tensor([0.0, -0.0, 448.0, -448.0])])
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.f64_to_e4m3fn(x.double().numpy()), ref)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    got = O.f64_to_e4m3fn(np.array([449.0, 464.0, 500.0, 1e30, np.inf, -np.inf, -1e6, np.nan, -np.nan]))
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F, 0x7F]
+    # ties to even: 1.0625 lies halfway between 1.0 (0x38) and 1.125 (0x39)
+    assert O.f64_to_e4m3fn(np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -11])).tolist() == [0x38, 0x3A, 0x00, 0x01]
+
+
+def test_kv_append_writes_the_slots_and_only_them():
+    g = torch.Generator().manual_seed(9)
+    pool, T = 40, 6
+    kv = torch.randint(0, 255, (pool, 576), generator=g, dtype=torch.uint8).numpy()
+    kv_c = (torch.randn(T, 512, generator=g) * 2).to(torch.bfloat16)
+    k_pe = (torch.randn(T, 64, generator=g) * 2).to(torch.bfloat16)
+    slots = np.array([3, -1, 17, 0, -5, 39], np.int64)
+    ks = 0.8
+    new = O.kv_append(kv, bf16_bits(kv_c), bf16_bits(k_pe), slots, ks)
+    untouched = np.setdiff1d(np.arange(pool), slots[slots >= 0])
+    assert np.array_equal(new[untouched], kv[untouched])
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        x = torch.cat([kv_c[i], k_pe[i]]).float() / ks            # float32 quotient
+        assert np.array_equal(new[s], x.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    # read back through the decoder: within half an e4m3 step of the value
+    back = O.dequant(new[slots[0]], ks)
+    ref = torch.cat([kv_c[0], k_pe[0]]).double().numpy()
+    assert np.all(np.abs(back - ref) <= np.abs(ref) * 2.0 ** -4 + 2.0 ** -10 * ks)
