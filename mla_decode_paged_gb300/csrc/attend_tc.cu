@@ -450,6 +450,37 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
     if (lane == 0) mbar_arrive(&ms.q_ready);
 }
 
+// p = 2^(s - m) of a thread's H2 scores, added to the row sums l and split
+// into e4m3 hi + lo/16 (hi = p rounded to 3 mantissa bits in fp32, exact in
+// e4m3; lo = 16 * (p - hi)), packed four columns per word.  GUARD maps
+// s = -inf to 0 even where m is still -inf (causal tiles; without the mask
+// every column sees each tile's live tokens, so m is finite by then).
+template <int H2, bool GUARD>
+__device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)[H2], float (&l)[H2],
+                                        uint32_t (&ph)[H2 / 4], uint32_t (&pl)[H2 / 4]) {
+#pragma unroll
+    for (int j = 0; j < H2; j += 2) {
+        float hv[2], lv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2f(sc[j + e] - mr[j + e]) : 0.f;
+            l[j + e] += pv;
+            hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
+            lv[e] = (pv - hv[e]) * 16.f;
+        }
+        const uint32_t h8 = __nv_cvt_float2_to_fp8x2(make_float2(hv[0], hv[1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t l8 = __nv_cvt_float2_to_fp8x2(make_float2(lv[0], lv[1]), __NV_SATFINITE, __NV_E4M3);
+        const int wi = j >> 2;
+        if ((j & 2) == 0) {
+            ph[wi] = h8;
+            pl[wi] = l8;
+        } else {
+            ph[wi] |= h8 << 16;
+            pl[wi] |= l8 << 16;
+        }
+    }
+}
+
 // Softmax warpgroups: thread (warpgroup g, TMEM lane t) owns token t of the
 // tile (latent row t of O in the epilogue) and query columns
 // [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale), c/16 and
@@ -467,6 +498,7 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
     const int S = P.R * P.qlen, rows_total = P.qlen * P.heads;
     float l[H2], cr[H2], c16[H2], mr[H2];
     int n_s = 0, n_units = 0;
+    int vmin = 0;   // causal: tokens of the request every query row sees (L_r - qlen + 1)
     uint8_t *prow = sm + C::OffP + (t >> 3) * 1024 + (t & 7) * 128;
     // The first unit's query is prepared while its first tile is loading;
     // later ones at the end of the unit before them.
@@ -514,8 +546,13 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
                 }
             }
             // vis[] is read below by every softmax thread in this same tile
-            if (CAUSAL) named_sync(kSoftBar, kSoftThreads);
+            if (CAUSAL) {
+                vmin = __ldg(P.indptr + M.r + 1) - __ldg(P.indptr + M.r) - P.qlen + 1;
+                named_sync(kSoftBar, kSoftThreads);
+            }
         }
+        // Only a tile that reaches past vmin needs the per-column mask.
+        const bool mask_tile = CAUSAL && M.tok0 + M.ntok > vmin;
         // ---- scores (log2 domain) of this thread's token and columns
         if (!wait_or_abort(&ms.s_full, n_s & 1, &ms.abort_flag)) return;
         ++n_s;
@@ -528,12 +565,19 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
             ld_cols<H2>(tm + NQ + n0, lo);
             tc::wait_ld();
             const bool live = t < M.ntok;
-            const int pos = M.tok0 + t;   // token position in the request
+            if (!mask_tile) {
 #pragma unroll
-            for (int j = 0; j < H2; ++j) {
-                const bool seen = CAUSAL ? live && pos < ms.vis[n0 + j] : live;
-                sc[j] = seen ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
-                over |= sc[j] - mr[j] > kRebase;   // also true for every live token while m = -inf
+                for (int j = 0; j < H2; ++j) {
+                    sc[j] = live ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                    over |= sc[j] - mr[j] > kRebase;   // also true for every live token while m = -inf
+                }
+            } else {
+                const int pos = M.tok0 + t;   // token position in the request
+#pragma unroll
+                for (int j = 0; j < H2; ++j) {
+                    sc[j] = live && pos < ms.vis[n0 + j] ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                    over |= sc[j] - mr[j] > kRebase;
+                }
             }
         }
         // ---- lazy reference max (rare after a unit's first tile)
@@ -583,29 +627,8 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
         // mantissa bits in fp32 (exact in e4m3), lo = 16 * (p - hi); this
         // thread's bytes of row t of P'^T
         uint32_t ph[H2 / 4], pl[H2 / 4];
-#pragma unroll
-        for (int j = 0; j < H2; j += 2) {
-            float hv[2], lv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                // masked entries give 0 even while the column's m is still -inf
-                // (without the mask every column sees each tile's live tokens)
-                const float pv = (!CAUSAL || sc[j + e] > -INFINITY) ? exp2f(sc[j + e] - mr[j + e]) : 0.f;
-                l[j + e] += pv;
-                hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
-                lv[e] = (pv - hv[e]) * 16.f;
-            }
-            const uint32_t h8 = __nv_cvt_float2_to_fp8x2(make_float2(hv[0], hv[1]), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t l8 = __nv_cvt_float2_to_fp8x2(make_float2(lv[0], lv[1]), __NV_SATFINITE, __NV_E4M3);
-            const int wi = j >> 2;
-            if ((j & 2) == 0) {
-                ph[wi] = h8;
-                pl[wi] = l8;
-            } else {
-                ph[wi] |= h8 << 16;
-                pl[wi] |= l8 << 16;
-            }
-        }
+        if (!mask_tile) p_split<H2, false>(sc, mr, l, ph, pl);
+        else p_split<H2, true>(sc, mr, l, ph, pl);   // masked entries: 0 even while a column's m is -inf
 #pragma unroll
         for (int g = 0; g < H2 / 8; ++g) {
             const int bh = n0 + 8 * g, bl = NQ + n0 + 8 * g;   // byte offsets in the 128-byte row
