@@ -294,6 +294,7 @@ def run_gpu(args):
         e_t.append(a.elapsed_time(b) * 1e-3)
     e2e_total = sum(e_t)
     ok = torch.equal(out_h, out.cpu())
+    extra = _time_kv_append(inp, S, flush, dev, stream, args.warmup, min(args.steps, 200))
 
     if ws > 1:
         total, e2e_total = max_over_ranks([total, e2e_total], dev)
@@ -342,11 +343,42 @@ def run_gpu(args):
         "e2e": {"value": aggregate_value(S, args.steps, ws, e2e_total), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "output_matches_device": bool(ok)},
         "gpu_launches": (3 if args.three_call else 2) * args.steps,
+        "extra_ops": extra,
         "clocks": clk,
     }
     if ws == 1 and not args.no_cpu_baseline:
         rec["cpu_baseline"] = cpu_baseline(spec, inp)
     return rec
+
+
+def _time_kv_append(inp, S, flush, dev, stream, warmup, steps):
+    """The cache write of new tokens (not part of the timed step): one new
+    token per query row (decode), and a 65,536-token batch (bandwidth).
+    Runs after everything else (it overwrites cache rows)."""
+    res = {}
+    pool = inp.kv.shape[0]
+    g = torch.Generator(device=dev).manual_seed(77)
+    for name, T in (("decode_tokens", S), ("batch_65536", min(65536, pool))):
+        kv_c = torch.randn(T, 512, generator=g, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn(T, 64, generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(pool, generator=g, device=dev)[:T].to(torch.int64)
+        for _ in range(warmup):
+            mla.kv_append(inp.kv, kv_c, k_pe, slots, inp.kv_scale, stream=stream)
+        ts = []
+        for _ in range(steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            mla.kv_append(inp.kv, kv_c, k_pe, slots, inp.kv_scale, stream=stream)
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        t = statistics.mean(a.elapsed_time(b) * 1e-3 for a, b in ts)
+        nbytes = T * (512 * 2 + 64 * 2 + 8 + 576)
+        res["kv_append_" + name] = {"tokens": T, "us": t * 1e6, "bytes": nbytes, "GB/s": nbytes / t / 1e9}
+    if mla.device_status():
+        raise SystemExit("device status flags after kv_append")
+    return res
 
 
 def _ncu_traffic(workload):

@@ -190,6 +190,32 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
                                 int heads, void *out, void *latent, float *lse_out, void *stream);
 
 /*
+ * mla_kv_append -- write new tokens into the fp8 latent cache.
+ *
+ * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla, pre
+ * (do_kv_cache_update: each new token's kv_c (512 latent values) and k_pe
+ * (64 rope values) are stored, scaled by 1/_k_scale and converted to fp8,
+ * at the token's slot of the flat token rows that mla_decode_attend reads).
+ * For token i with slots[i] >= 0 and every d < 576:
+ *   kv[slots[i], d] = e4m3(x / k_scale),  x = kv_c[i, d] (d < 512) or k_pe[i, d - 512]
+ * with the quotient in float32 (IEEE division) and e4m3 round-to-nearest-
+ * even, saturating (magnitudes above 448 and infinities give +-448, NaN
+ * stays NaN).  A negative slot skips its token (padding).  Two tokens with
+ * the same slot: which one lands is unspecified.
+ *
+ *   kv_c         bf16, token i at kv_c + i*kv_c_row_stride (elements, >= 512,
+ *                multiple of 8).
+ *   k_pe         bf16, token i at k_pe + i*k_pe_row_stride (>= 64, multiple of 8).
+ *   slots        int64 [num_tokens], device memory.
+ *   kv           fp8 codes [pool_rows, 576] (written at the slots only).
+ * Slots >= pool_rows are skipped and set MLA_DEV_BAD_PAGE.  k_scale must be
+ * finite and > 0.  kv_c, k_pe, kv 16-byte aligned; slots 8-byte aligned.
+ */
+mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *k_pe, int64_t k_pe_row_stride,
+                         const int64_t *slots, int64_t num_tokens, float k_scale, void *kv, int64_t pool_rows,
+                         void *stream);
+
+/*
  * mla_choose_splits -- a split plan for mla_decode_attend from host-known
  * sizes (no device read).  Returns num_splits (>= 1) and writes
  * *split_tokens.  The plan minimises a model of the attend time: work units

@@ -30,7 +30,7 @@ ATTEND_CAUSAL = 1
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
 
 __all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "debug_gather",
-           "device_status", "build", "library", "MlaError"]
+           "kv_append", "device_status", "build", "library", "MlaError"]
 
 
 class MlaError(RuntimeError):
@@ -71,8 +71,9 @@ def library() -> ctypes.CDLL:
     lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.mla_kv_append.argtypes = [vp, i64, vp, i64, vp, i64, f32, vp, i64, vp]
     for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
-                 "mla_device_status", "mla_choose_splits"):
+                 "mla_device_status", "mla_choose_splits", "mla_kv_append"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -243,6 +244,29 @@ def debug_gather(kv, pages, indptr, total_rows=None, stream=None):
                                     indptr.numel() - 1, total_rows, _ptr(out), ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_debug_gather")
     return out
+
+
+def kv_append(kv, kv_c, k_pe, slots, k_scale, *, stream=None):
+    """Write new tokens into the fp8 cache in place: ``kv[slots[i]] =
+    e4m3((kv_c[i] ++ k_pe[i]) / k_scale)`` (negative slots skipped).
+
+    ``kv``: uint8 / float8_e4m3fn ``[pool, 576]``; ``kv_c``: bf16 ``[T, 512]``
+    and ``k_pe``: bf16 ``[T, 64]`` (rows may be strided); ``slots``: int64
+    ``[T]``.  Returns ``kv``.
+    """
+    kvu = _as_u8(kv)
+    _need(kvu.dim() == 2 and kvu.shape[1] == D_QK and kvu.is_contiguous(), "kv must be contiguous [pool, 576]")
+    _need(kv_c.dtype == torch.bfloat16 and kv_c.dim() == 2 and kv_c.shape[1] == D_LATENT and kv_c.stride(1) == 1,
+          "kv_c must be bf16 [T, 512] with contiguous rows")
+    _need(k_pe.dtype == torch.bfloat16 and k_pe.dim() == 2 and k_pe.shape[1] == D_QK - D_LATENT and k_pe.stride(1) == 1,
+          "k_pe must be bf16 [T, 64] with contiguous rows")
+    T = kv_c.shape[0]
+    _need(k_pe.shape[0] == T and slots.dtype == torch.int64 and slots.numel() == T and slots.is_contiguous(),
+          "slots must be contiguous int64 [T] matching kv_c / k_pe")
+    st = library().mla_kv_append(_ptr(kv_c), kv_c.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(slots), T,
+                                 float(k_scale), _ptr(kvu), kvu.shape[0], ctypes.c_void_p(_stream(stream)))
+    _check(st, "mla_kv_append")
+    return kv
 
 
 def device_status(stream=None) -> int:

@@ -36,6 +36,10 @@ cudaError_t merge_value_status(unsigned int *flags, bool clear);
 cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
                           int R, int64_t total_rows, void *out, cudaStream_t st);
 cudaError_t gather_status(unsigned int *flags, bool clear);
+cudaError_t kv_append_launch(const void *kv_c, int64_t kv_c_stride, const void *k_pe, int64_t k_pe_stride,
+                             const int64_t *slots, int64_t T, float k_scale, void *kv, int64_t pool_rows, int sms,
+                             cudaStream_t st);
+cudaError_t kv_append_status(unsigned int *flags, bool clear);
 }  // namespace mla
 
 namespace {
@@ -244,6 +248,26 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
     return best_ns;
 }
 
+mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *k_pe, int64_t k_pe_row_stride,
+                         const int64_t *slots, int64_t num_tokens, float k_scale, void *kv, int64_t pool_rows,
+                         void *stream) {
+    if (num_tokens < 0 || pool_rows < 0) return fail(MLA_ERR_INVALID, "negative size");
+    if (kv_c_row_stride < MLA_D_LATENT || kv_c_row_stride % 8 != 0)
+        return fail(MLA_ERR_INVALID, "kv_c_row_stride must be >= 512 and a multiple of 8");
+    if (k_pe_row_stride < MLA_D_ROPE || k_pe_row_stride % 8 != 0)
+        return fail(MLA_ERR_INVALID, "k_pe_row_stride must be >= 64 and a multiple of 8");
+    if (!std::isfinite(k_scale) || !(k_scale > 0.f)) return fail(MLA_ERR_INVALID, "k_scale must be finite and > 0");
+    if (num_tokens == 0) return MLA_OK;
+    if (!kv_c || !k_pe || !slots || !kv) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(kv, 16) || !aligned(slots, 8))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (kv_c, k_pe, kv need 16 bytes, slots 8)");
+    if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    cudaError_t e = mla::kv_append_launch(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slots, num_tokens, k_scale,
+                                          kv, pool_rows, device_sms(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return MLA_OK;
+}
+
 mla_status mla_debug_gather(const void *kv, int64_t pool_rows, const int32_t *pages, int64_t num_pages,
                             const int32_t *indptr, int num_requests, int64_t total_rows, void *out,
                             void *stream) {
@@ -267,7 +291,8 @@ mla_status mla_device_status(void *stream, unsigned int *flags) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::attend_tc_status, mla::merge_status,
-                                                      mla::value_gate_status, mla::gather_status, mla::merge_value_status};
+                                                      mla::value_gate_status, mla::gather_status, mla::merge_value_status,
+                                                      mla::kv_append_status};
     for (auto rd : readers) {
         unsigned int f = 0;
         e = rd(&f, true);
