@@ -43,27 +43,39 @@
 namespace mla {
 namespace {
 
-constexpr int kT = 128;              // tokens per tile = MMA M
-constexpr int kStages = 2;
-constexpr int kStageBytes = 73728;   // 4 x (16 x 1024) latent + 16 x 512 rope
-constexpr int kRopeOff = 65536;
 constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarp0 = 9, kProdWarps = 7;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kThreads = (kSoftWarps + 1 + kProdWarps) * 32;
-constexpr int kOps = 160;            // gather4 ops per tile: 32 groups of 4 rows x (4 latent + 1 rope)
 constexpr int kSoftBar = 1;          // named barrier of the two softmax warpgroups
 constexpr float kRebase = 8.f;       // log2 headroom before the reference max moves
 
+// Tile shape and shared-memory layout per row count NQ: two 128-token
+// stages.  (The layout also admits shorter tiles -- a 96-token tile still
+// runs M = 128 QK^T MMAs that read 32 rows past it, inside the CTA's
+// allocation, with those score lanes ignored -- e.g. three 96-token stages
+// at 16 rows; on GB300 that measured slower, the per-tile MMA and sync
+// costs being fixed.)
 template <int NQ>
 struct Cfg {
+    static constexpr int T = 128;                          // tokens per tile
+    static constexpr int STAGES = 2;
+    static constexpr int Blk = (T / 8) * 1024;             // one 128-byte latent column block of a stage
+    static constexpr int RopeOff = 4 * Blk;                // rope bytes, 64B swizzle
+    static constexpr int StageBytes = RopeOff + (T / 8) * 512;
+    static constexpr int KSteps = T / 32;                  // P.V MMAs (K = 32 tokens) per latent block
+    static constexpr int Ops = (T / 4) * 5;                // gather4 ops: 4-row groups x (4 latent + 1 rope)
     static constexpr int NP = 2 * NQ;                      // MMA N (hi and lo terms)
     static constexpr int HALF = NQ / 2;                    // columns per softmax warpgroup
-    static constexpr int OffQ = kStages * kStageBytes;
+    static constexpr int OffQ = STAGES * StageBytes;
     static constexpr int QLatBlock = (NP / 8) * 1024;      // one 128-byte column block of Q'
     static constexpr int QRope = 4 * QLatBlock;
     static constexpr int OffP = OffQ + NP * 576;
-    static constexpr int OffMisc = OffP + 16384;
+    static constexpr int PBytes = (T / 8) * 1024;          // P'^T: one 128-byte row per token
+    static constexpr int OffMisc = OffP + PBytes;
     static constexpr uint32_t TmemCols = (10 * NQ <= 256) ? 256 : 512;
+    static_assert(T % 32 == 0 && T <= 128, "whole P.V K-steps, at most the MMA M");
+    static_assert(Ops <= kProdWarps * 32, "one gather4 per producer lane");
+    static_assert(NP <= 128, "a P' row is one 128-byte swizzle span");
 };
 
 // Descriptor of the tile in a stage (and of the tile after it), written by
@@ -78,9 +90,9 @@ constexpr int kMetaDone = 4, kNxtValid = 16;
 
 template <int NQ>
 struct Misc {
-    TileMeta meta[kStages];
+    TileMeta meta[Cfg<NQ>::STAGES];
     int64_t orow[NQ];       // o row (element offset / 512) of each query column, -1 for padding
-    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t kv_full[Cfg<NQ>::STAGES], kv_empty[Cfg<NQ>::STAGES];
     uint64_t s_full, p_full, q_ready, o_done, fin;
     uint32_t tmem;
     int abort_flag;
@@ -196,12 +208,13 @@ __device__ __forceinline__ void colsum(float *v, int lane, int &base) {
 
 template <int NQ>
 __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtensorMap *mrope, uint8_t *sm) {
+    using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int lane = threadIdx.x & 31, pw = (threadIdx.x >> 5) - kProdWarp0;
     const int op = pw + kProdWarps * lane;  // ops dealt round-robin over the producer warps
-    const bool has_op = op < kOps;
+    const bool has_op = op < C::Ops;
     const int g4 = op / 5, part = op % 5;
-    TileIter<kT> iter;
+    TileIter<C::T> iter;
     iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
@@ -243,8 +256,8 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
                 }
             }
         }
-        const int s = it % kStages;
-        if (!wait_or_abort(&ms.kv_empty[s], ((it / kStages) & 1) ^ 1, &ms.abort_flag)) return;
+        const int s = it % C::STAGES;
+        if (!wait_or_abort(&ms.kv_empty[s], ((it / C::STAGES) & 1) ^ 1, &ms.abort_flag)) return;
         const bool issue = has_op && cur.ntok > 0;
         uint32_t bytes = issue ? (part < 4 ? 512u : 256u) : 0u;
 #pragma unroll
@@ -261,13 +274,13 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
         }
         __syncwarp();
         if (issue) {
-            uint8_t *st = sm + s * kStageBytes;
+            uint8_t *st = sm + s * C::StageBytes;
             const int g8 = g4 >> 1, half = g4 & 1;
             if (part < 4)
-                tc::gather4(st + part * 16384 + g8 * 1024 + half * 512, mlat, part * 128, rows[0], rows[1], rows[2],
+                tc::gather4(st + part * C::Blk + g8 * 1024 + half * 512, mlat, part * 128, rows[0], rows[1], rows[2],
                             rows[3], &ms.kv_full[s]);
             else
-                tc::gather4(st + kRopeOff + g8 * 512 + half * 256, mrope, 512, rows[0], rows[1], rows[2], rows[3],
+                tc::gather4(st + C::RopeOff + g8 * 512 + half * 256, mrope, 512, rows[0], rows[1], rows[2], rows[3],
                             &ms.kv_full[s]);
         }
         cur = nxt;
@@ -276,8 +289,8 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
         n_issued = it + 1;
     }
     // No more work: one last "done" descriptor through the next stage.
-    const int s2 = n_issued % kStages;
-    if (!wait_or_abort(&ms.kv_empty[s2], ((n_issued / kStages) & 1) ^ 1, &ms.abort_flag)) return;
+    const int s2 = n_issued % C::STAGES;
+    if (!wait_or_abort(&ms.kv_empty[s2], ((n_issued / C::STAGES) & 1) ^ 1, &ms.abort_flag)) return;
     if (lane == 0) {
         if (pw == 0) ms.meta[s2].flags = kMetaDone;
         mbar_arrive(&ms.kv_full[s2]);
@@ -301,8 +314,8 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
     int n_p = 0, n_units = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
-        const int s = it % kStages;
-        if (!(ok = wait_or_abort(&ms.kv_full[s], (it / kStages) & 1, &ms.abort_flag))) break;
+        const int s = it % C::STAGES;
+        if (!(ok = wait_or_abort(&ms.kv_full[s], (it / C::STAGES) & 1, &ms.abort_flag))) break;
         const TileMeta M = ms.meta[s];
         if (M.flags & kMetaDone) break;
         if (M.ntok == 0) {
@@ -318,17 +331,17 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
             ++n_units;
         }
         tc::fence_after();
-        const uint32_t st = base + s * kStageBytes;
+        const uint32_t st = base + s * C::StageBytes;
         if (lane == 0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int a = j >> 2, off = (j & 3) * 32;
-                tc::mma_e4m3(tm, tc::sdesc(st + a * 16384 + off, 16, 1024, tc::kSw128),
+                tc::mma_e4m3(tm, tc::sdesc(st + a * C::Blk + off, 16, 1024, tc::kSw128),
                              tc::sdesc(base + C::OffQ + a * C::QLatBlock + off, 16, 1024, tc::kSw128), kIdQK, j > 0);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-                tc::mma_e4m3(tm, tc::sdesc(st + kRopeOff + j * 32, 16, 512, tc::kSw64),
+                tc::mma_e4m3(tm, tc::sdesc(st + C::RopeOff + j * 32, 16, 512, tc::kSw64),
                              tc::sdesc(base + C::OffQ + C::QRope + j * 32, 16, 512, tc::kSw64), kIdQK, true);
             tc::commit(&ms.s_full);
         }
@@ -337,11 +350,11 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
         tc::fence_after();
         if (lane == 0) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < C::KSteps; ++kk)
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
-                    tc::mma_e4m3(tm + C::NP * (1 + b), tc::sdesc(st + b * 16384 + kk * 4096, 16384, 1024, tc::kSw128),
-                                 tc::sdesc(base + C::OffP + kk * 4096, 16384, 1024, tc::kSw128), kIdPV,
+                    tc::mma_e4m3(tm + C::NP * (1 + b), tc::sdesc(st + b * C::Blk + kk * 4096, C::Blk, 1024, tc::kSw128),
+                                 tc::sdesc(base + C::OffP + kk * 4096, C::Blk, 1024, tc::kSw128), kIdPV,
                                  !(first && kk == 0));
             tc::commit(&ms.kv_empty[s]);
             if (M.flags & kTileLast) tc::commit(&ms.o_done);
@@ -505,8 +518,8 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
     if (!wait_or_abort(&ms.first_ready, 0, &ms.abort_flag)) return;
     if (!(ms.first[2] & kMetaDone) && ms.first[1] > 0) prep_query<NQ>(P, sm, ms.first[0], ms.first[2] >> 8);
     for (int it = 0;; ++it) {
-        const int s = it % kStages;
-        if (!wait_or_abort(&ms.kv_full[s], (it / kStages) & 1, &ms.abort_flag)) return;
+        const int s = it % C::STAGES;
+        if (!wait_or_abort(&ms.kv_full[s], (it / C::STAGES) & 1, &ms.abort_flag)) return;
         const TileMeta M = ms.meta[s];
         __syncwarp();
         if (M.flags & kMetaDone) return;
@@ -629,11 +642,13 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
         uint32_t ph[H2 / 4], pl[H2 / 4];
         if (!mask_tile) p_split<H2, false>(sc, mr, l, ph, pl);
         else p_split<H2, true>(sc, mr, l, ph, pl);   // masked entries: 0 even while a column's m is -inf
+        if (C::T == 128 || t < C::T) {   // lanes past a shorter tile have no P' row
 #pragma unroll
-        for (int g = 0; g < H2 / 8; ++g) {
-            const int bh = n0 + 8 * g, bl = NQ + n0 + 8 * g;   // byte offsets in the 128-byte row
-            *reinterpret_cast<uint2 *>(prow + ((((bh >> 4) ^ t) & 7) << 4) + (bh & 15)) = make_uint2(ph[2 * g], ph[2 * g + 1]);
-            *reinterpret_cast<uint2 *>(prow + ((((bl >> 4) ^ t) & 7) << 4) + (bl & 15)) = make_uint2(pl[2 * g], pl[2 * g + 1]);
+            for (int g = 0; g < H2 / 8; ++g) {
+                const int bh = n0 + 8 * g, bl = NQ + n0 + 8 * g;   // byte offsets in the 128-byte row
+                *reinterpret_cast<uint2 *>(prow + ((((bh >> 4) ^ t) & 7) << 4) + (bh & 15)) = make_uint2(ph[2 * g], ph[2 * g + 1]);
+                *reinterpret_cast<uint2 *>(prow + ((((bl >> 4) ^ t) & 7) << 4) + (bl & 15)) = make_uint2(pl[2 * g], pl[2 * g + 1]);
+            }
         }
         tc::fence_async_smem();
         tc::fence_before();
@@ -678,7 +693,8 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
 #pragma unroll
             for (int j = 0; j < H2; ++j) iv[j] = ms.invl[n0 + j];
             __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + C::OffP);
-            constexpr int kBlkRound = 16384 / (NQ * 256);   // latent blocks staged at a time
+            // latent blocks staged at a time (4, 2 or 1: a divisor of 4)
+            constexpr int kBlkRound = 4 * NQ * 256 <= C::PBytes ? 4 : 2 * NQ * 256 <= C::PBytes ? 2 : 1;
 #pragma unroll 1
             for (int b0 = 0; b0 < 4; b0 += kBlkRound) {
 #pragma unroll 1
@@ -715,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Misc<NQ> &ms = misc<NQ>(sm);
     const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < Cfg<NQ>::STAGES; ++s) {
             mbar_init(&ms.kv_full[s], kProdWarps);
             // released by the softmax warps' read of the descriptor and the MMA warp
             mbar_init(&ms.kv_empty[s], kSoftWarps + 1);
@@ -733,6 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // Every CTA is resident (one per SM): a kernel launched after this one
+    // with programmatic dependent launch may start on SMs as they free up;
+    // it waits for this grid's completion before reading its results.
+    asm volatile("griddepcontrol.launch_dependents;");
     // Register split (per warpgroup; 512 x 128 at launch): the two softmax
     // warpgroups take 184, the MMA / producer warpgroups 72.
     // 256 x 184 + 256 x 72 = 65536.

@@ -18,6 +18,10 @@
 // the gate epilogue.  COLS = 32: four CTAs per row tile, so a small batch
 // still spreads over the SMs (the host routes large batches to the
 // separate merge and value kernels, which read each partial row once).
+// Launched with programmatic dependent launch: the W_UV copies and the gate
+// loads (inputs no earlier kernel writes) start while the attend grid is
+// still finishing; griddepcontrol.wait orders every read of the partials
+// and every global write after that grid's completion.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -151,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1) merge_value_kernel(
             if (active[hh]) gw[hh] = __ldg(reinterpret_cast<const uint32_t *>(gate + rowoff + 8 * warp + 2 * qd));
         }
     }
+    // The partials come from the previous grid on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // One latent row per warp into smem.
     {
         const long long nrow = (long long)S * H;
@@ -198,12 +204,20 @@ cudaError_t launch(const void *o, const float *lse, int num_splits, const void *
     const size_t smem = sizeof(Smem<COLS>);
     cudaError_t e = cudaFuncSetAttribute(merge_value_kernel<COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((S + kRows - 1) / kRows, H, MLA_D_V / COLS);
-    merge_value_kernel<COLS><<<grid, kThreads, smem, st>>>(
-        static_cast<const __nv_bfloat16 *>(o), lse, num_splits, static_cast<const __nv_bfloat16 *>(w_uv),
-        static_cast<const __nv_bfloat16 *>(gate), lengths, S, qlen, H, static_cast<__nv_bfloat16 *>(out),
-        static_cast<__nv_bfloat16 *>(latent), lse_out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((S + kRows - 1) / kRows, H, MLA_D_V / COLS);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_value_kernel<COLS>, static_cast<const __nv_bfloat16 *>(o), lse, num_splits,
+                              static_cast<const __nv_bfloat16 *>(w_uv), static_cast<const __nv_bfloat16 *>(gate),
+                              lengths, S, qlen, H, static_cast<__nv_bfloat16 *>(out),
+                              static_cast<__nv_bfloat16 *>(latent), lse_out);
 }
 
 }  // namespace
