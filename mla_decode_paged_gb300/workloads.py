@@ -214,3 +214,33 @@ def make_partials(splits: int, rows: int, heads: int, seed: int, device="cpu",
     lse[drop] = float("-inf")
     o[drop] = float("nan")
     return o, lse
+
+def make_block_inputs(spec: WorkloadSpec | int, device="cpu", page_size: int = 16, lengths=None) -> Inputs:
+    """A workload's tensors with the KV cache in block-table form (vLLM's
+    paged layout with ``page_size`` rows per block): the pool holds whole
+    blocks, each request owns ceil(L_r / page_size) distinct random blocks,
+    ``pages`` lists block indices, ``indptr`` counts blocks and
+    ``extra['last_page_len']`` (int32 [R]) is how many rows of each
+    request's last block are used (0 for an empty request).
+    ``extra['page_size']`` records the block size.  q, W_UV, gate and the
+    value distributions are those of :func:`make_inputs`."""
+    if isinstance(spec, int):
+        spec = WORKLOADS[spec]
+    base = make_inputs(spec, "cpu", lengths=lengths)
+    lens = base.lengths.to(torch.int64)
+    R = int(lens.numel())
+    nb = (lens + page_size - 1) // page_size
+    total_blocks = int(nb.sum().item())
+    g = torch.Generator().manual_seed(2000 + spec.seed)
+    pool_blocks = max(total_blocks + 3, 1)
+    blocks = torch.randperm(pool_blocks, generator=g)[:total_blocks].to(torch.int32)
+    indptr = torch.zeros(R + 1, dtype=torch.int64)
+    indptr[1:] = torch.cumsum(nb, 0)
+    last = torch.where(nb > 0, lens - (nb - 1) * page_size, torch.zeros_like(lens)).to(torch.int32)
+    kv = _randn_fp8_codes(pool_blocks * page_size, g, "cpu", 0.5)
+    device = torch.device(device)
+    out = Inputs(base.spec, base.q.to(device), kv.to(device), blocks.to(device), indptr.to(torch.int32).to(device),
+                 base.lengths.to(device), base.w_uv.to(device), base.gate.to(device), base.scale, base.kv_scale)
+    out.extra["page_size"] = page_size
+    out.extra["last_page_len"] = last.to(device)
+    return out

@@ -85,20 +85,39 @@ def sigmoid(x) -> np.ndarray:
 # Paged gather
 # ---------------------------------------------------------------------------
 
-def gather_rows(kv_codes, pages, indptr, r: int) -> np.ndarray:
-    """Request r's KV rows, as raw fp8 codes [L_r, 576]: the flat token rows
-    ``kv.view(-1, 576)`` addressed by ``pages[indptr[r]:indptr[r+1]]``
-    (``m1c_inputs``: ``kv``, ``pages``, ``indptr``; page size 1)."""
-    kv_codes = np.asarray(kv_codes, dtype=np.uint8)
+def request_rows(pages, indptr, r: int, page_size: int = 1, last_page_len=None) -> np.ndarray:
+    """Row indices of request r's tokens in the flat token rows, in order.
+
+    Page size 1 (``m1c_inputs``: "the flat token rows"): ``pages[indptr[r]:
+    indptr[r+1]]``.  Page size P > 1 (vLLM block tables): ``pages`` holds
+    block indices and ``indptr`` counts blocks; block b covers rows
+    [b*P, (b+1)*P); the request's last block holds ``last_page_len[r]``
+    tokens, so L_r = (blocks - 1) * P + last_page_len[r] and token j is row
+    ``pages[indptr[r] + j // P] * P + j % P``.
+    """
     lo, hi = int(indptr[r]), int(indptr[r + 1])
-    idx = np.asarray(pages[lo:hi], dtype=np.int64)
-    return kv_codes[idx]
+    blocks = np.asarray(pages[lo:hi], dtype=np.int64)
+    if page_size == 1:
+        return blocks
+    if blocks.size == 0:
+        return blocks
+    L = (blocks.size - 1) * page_size + int(last_page_len[r])
+    j = np.arange(L, dtype=np.int64)
+    return blocks[j // page_size] * page_size + j % page_size
 
 
-def gather_all(kv_codes, pages, indptr) -> np.ndarray:
+def gather_rows(kv_codes, pages, indptr, r: int, page_size: int = 1, last_page_len=None) -> np.ndarray:
+    """Request r's KV rows, as raw fp8 codes [L_r, 576]: the flat token rows
+    ``kv.view(-1, 576)`` addressed through :func:`request_rows`
+    (``m1c_inputs``: ``kv``, ``pages``, ``indptr``)."""
+    kv_codes = np.asarray(kv_codes, dtype=np.uint8)
+    return kv_codes[request_rows(pages, indptr, r, page_size, last_page_len)]
+
+
+def gather_all(kv_codes, pages, indptr, page_size: int = 1, last_page_len=None) -> np.ndarray:
     """Every request's rows, concatenated in request order: [sum L, 576]."""
     R = len(indptr) - 1
-    parts = [gather_rows(kv_codes, pages, indptr, r) for r in range(R)]
+    parts = [gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len) for r in range(R)]
     if not parts:
         return np.zeros((0, D_QK), np.uint8)
     return np.concatenate(parts, axis=0)
@@ -160,7 +179,7 @@ def dequant(codes, kv_scale: float) -> np.ndarray:
 
 
 def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-           requests=None, return_p=False, causal=False):
+           requests=None, return_p=False, causal=False, page_size=1, last_page_len=None):
     """The unsplit attention: latent [S, H, 512] and LSE [S, H].
 
     ``q_bits``: uint16 bf16 bits [S, H_pad, 576]; only heads < ``heads`` are
@@ -168,6 +187,7 @@ def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     ``requests``: optional subset of request indices to compute (others are
     left NaN), so that full-size workloads can be checked on a sample.
     ``causal``: apply :func:`causal_visible` to each request's rows.
+    ``page_size`` / ``last_page_len``: block tables (:func:`request_rows`).
     """
     q = np.asarray(q_bits)
     R = len(indptr) - 1
@@ -176,7 +196,7 @@ def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     lse = np.full((S, heads), np.nan)
     ps = {}
     for r in (range(R) if requests is None else requests):
-        K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
+        K = dequant(gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len), kv_scale)
         rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
         vis = causal_visible(K.shape[0], qlen, heads) if causal else None
         lat, l, p = attend_rows(rows, K, scale, vis)
@@ -216,7 +236,7 @@ def split_plan(L: int, num_splits: int, split_tokens: int):
 
 
 def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                  num_splits, split_tokens, requests=None, causal=False):
+                  num_splits, split_tokens, requests=None, causal=False, page_size=1, last_page_len=None):
     """Per-split partials: o [num_splits, S, H, 512] (float64) and lse
     [num_splits, S, H]; each used split is the attention restricted to its
     token range (``m1c_inputs``: new partials o [splits, S, 12, 512], LSE
@@ -233,7 +253,7 @@ def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
         lse[:] = np.nan
     for r in (range(R) if requests is None else requests):
         lse[:, r * qlen:(r + 1) * qlen] = -np.inf
-        K = dequant(gather_rows(kv_codes, pages, indptr, r), kv_scale)
+        K = dequant(gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len), kv_scale)
         rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
         vis = causal_visible(K.shape[0], qlen, heads) if causal else np.full(qlen * heads, K.shape[0])
         for k, (a, b) in enumerate(split_plan(K.shape[0], num_splits, split_tokens)):
@@ -302,11 +322,11 @@ def value_gate(latent, w_uv_bits, gate_bits, lengths, qlen):
 
 
 def decode_step(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                w_uv_bits, gate_bits, lengths, requests=None, causal=False):
+                w_uv_bits, gate_bits, lengths, requests=None, causal=False, page_size=1, last_page_len=None):
     """The whole step from raw inputs: (latent, lse, out).  With
     ``requests``, only those requests' rows are filled (the rest NaN)."""
     latent, lse = attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                         requests=requests, causal=causal)
+                         requests=requests, causal=causal, page_size=page_size, last_page_len=last_page_len)
     lat_in = np.nan_to_num(latent, nan=0.0)
     out = value_gate(lat_in, w_uv_bits, gate_bits, lengths, qlen)
     if requests is not None:

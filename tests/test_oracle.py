@@ -443,3 +443,36 @@ def test_kv_append_writes_the_slots_and_only_them():
     back = O.dequant(new[slots[0]], ks)
     ref = torch.cat([kv_c[0], k_pe[0]]).double().numpy()
     assert np.all(np.abs(back - ref) <= np.abs(ref) * 2.0 ** -4 + 2.0 ** -10 * ks)
+
+
+# ------------------------------------------------------------- block tables
+
+@pytest.mark.parametrize("P", [2, 16, 64])
+def test_block_table_rows_are_the_blocks_in_order(P):
+    """Request rows under a block table: the concatenated row ranges of the
+    request's blocks, cut to its length."""
+    inp = W.make_block_inputs(4, "cpu", page_size=P, lengths=[0, 1, P, P + 1, 3 * P - 1, 200])
+    pages, indptr = i32(inp.pages), i32(inp.indptr)
+    last = i32(inp.extra["last_page_len"])
+    lens = i32(inp.lengths)
+    for r in range(len(lens)):
+        blocks = pages[indptr[r]:indptr[r + 1]]
+        want = [row for b in blocks for row in range(int(b) * P, int(b) * P + P)][:lens[r]]
+        got = O.request_rows(pages, indptr, r, P, last)
+        assert got.tolist() == want
+
+
+@pytest.mark.parametrize("P", [4, 16])
+def test_block_table_attention_equals_flat_page_list(P):
+    inp = W.make_block_inputs(4, "cpu", page_size=P, lengths=[0, 5, 200, 333, 64])
+    a = oracle_args(inp)
+    last = i32(inp.extra["last_page_len"])
+    lat, lse = O.attend(**a, page_size=P, last_page_len=last)
+    rows = [O.request_rows(a["pages"], a["indptr"], r, P, last) for r in range(len(a["indptr"]) - 1)]
+    flat_indptr = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    flat = dict(a, pages=np.concatenate(rows).astype(np.int32), indptr=flat_indptr)
+    lat1, lse1 = O.attend(**flat)
+    assert np.array_equal(lat, lat1) and np.array_equal(lse, lse1)
+    o, ls = O.attend_splits(**a, num_splits=5, split_tokens=50, page_size=P, last_page_len=last)
+    o1, ls1 = O.attend_splits(**flat, num_splits=5, split_tokens=50)
+    assert np.array_equal(ls, ls1) and np.array_equal(np.nan_to_num(o, nan=7.0), np.nan_to_num(o1, nan=7.0))
