@@ -86,15 +86,17 @@ def _spec(name):
     raise SystemExit("unknown workload %s (have %s)" % (name, [s.name for s in W.WORKLOADS]))
 
 
-def _plan_stats(inp, ns, st):
-    """Host-side split counts and the attend kernel's algorithmic bytes."""
+def _plan_stats(inp, ns, st, page_size=1):
+    """Host-side split counts and the attend kernel's algorithmic bytes
+    (KV rows, page / block indices, indptr, q, partials)."""
     lens = inp.lengths.cpu().numpy().astype(np.int64)
     n_r = np.maximum(1, np.minimum(ns, -(-lens // st)))
     used = int(n_r[lens > 0].sum())
     rows_per_req = inp.qlen * inp.heads
     total = int(lens.sum())
     R = len(lens)
-    attend_bytes = (total * (576 + 4) + (R + 1) * 4 + R * rows_per_req * 576 * 2
+    index_bytes = 4 * total if page_size == 1 else 4 * int((-(-lens // page_size)).sum()) + 4 * R
+    attend_bytes = (total * 576 + index_bytes + (R + 1) * 4 + R * rows_per_req * 576 * 2
                     + used * rows_per_req * (512 * 2 + 4)
                     + int((ns - n_r).sum() + (lens == 0).sum()) * rows_per_req * 4)
     merge_bytes = used * rows_per_req * (512 * 2 + 4) + ns * R * rows_per_req * 4 + R * rows_per_req * (1024 + 4)
@@ -176,11 +178,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     mla.build()
     spec = _spec(args.workload)
-    inp = W.make_inputs(spec, dev)
+    inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
+    last = inp.extra.get("last_page_len")
     R, qlen, H = spec.requests, spec.qlen, spec.heads
     S = R * qlen
     ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
-    stats = _plan_stats(inp, ns, st)
+    stats = _plan_stats(inp, ns, st, args.page_size)
     stream = torch.cuda.current_stream(dev)
 
     o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
@@ -194,7 +197,7 @@ def run_gpu(args):
         if ev:
             ev[0].record(strm)
         mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, causal=args.causal, stream=strm)
+                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last, stream=strm)
         if ev:
             ev[1].record(strm)
         if args.three_call:
@@ -262,17 +265,21 @@ def run_gpu(args):
     pages_h = inp.pages.cpu().pin_memory()
     indptr_h = inp.indptr.cpu().pin_memory()
     lens_h = inp.lengths.cpu().pin_memory()
+    last_h = last.cpu().pin_memory() if last is not None else None
+    last_d = torch.empty_like(last) if last is not None else None
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     q_d, gate_d = torch.empty_like(inp.q), torch.empty_like(inp.gate)
     pages_d, indptr_d, lens_d = torch.empty_like(inp.pages), torch.empty_like(inp.indptr), torch.empty_like(inp.lengths)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h))
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h, last_h) if t is not None)
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
-        for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h)):
-            d.copy_(h, non_blocking=True)
+        for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h),
+                     (last_d, last_h)):
+            if d is not None:
+                d.copy_(h, non_blocking=True)
         mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, causal=args.causal, stream=stream)
+                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, stream=stream)
         if args.three_call:
             mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
             mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
@@ -324,7 +331,7 @@ def run_gpu(args):
             "num_splits": ns, "split_tokens": st, "work_units": stats["used_units"],
             "l2": "flushed before every timed step (256 MB write, outside the events)",
             "parallelism": "replicas" if ws > 1 else "single-gpu",
-            "kv": "fp8-e4m3 paged (page size 1)",
+            "kv": "fp8-e4m3 paged (page size %d%s)" % (args.page_size, ", block tables" if args.page_size > 1 else ""),
             "mask": "causal within a request" if args.causal else "none",
             "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 mma.sync (W_UV)",
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
@@ -480,6 +487,8 @@ def main():
     ap.add_argument("--three-call", action="store_true",
                     help="time merge and value/gate as two launches instead of the fused one")
     ap.add_argument("--ref-budget", type=float, default=5.0)
+    ap.add_argument("--page-size", type=int, default=1,
+                    help="KV cache as block tables of this many rows per block (power of two)")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     args = ap.parse_args()

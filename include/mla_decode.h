@@ -129,6 +129,32 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
                                 void *o, float *lse, unsigned int flags, void *stream);
 
 /*
+ * mla_decode_attend_paged -- mla_decode_attend_ex over a block-table cache.
+ *
+ * The pages address "the flat token rows" one row per entry (m1c_inputs:
+ * page size 1).  vLLM's paged layout groups page_size rows per block: here
+ * pages holds block indices, indptr[r+1] - indptr[r] counts request r's
+ * blocks, the last block holds last_page_len[r] rows, and token j of
+ * request r is the flat row
+ *   pages[indptr[r] + j / page_size] * page_size + j % page_size,
+ * so L_r = (blocks - 1) * page_size + last_page_len[r] (0 with no blocks).
+ * Everything else (split plan in tokens, outputs, flags) as
+ * mla_decode_attend_ex; page_size 1 ignores last_page_len (may be NULL).
+ *
+ *   page_size      power of two, 1..256; pool_rows a multiple of it.
+ *   last_page_len  int32 [num_requests], device, each in 1..page_size for a
+ *                  request with blocks (else MLA_DEV_BAD_INDPTR, request empty).
+ * A block index whose rows fall outside the pool sets MLA_DEV_BAD_PAGE.
+ * page_size > 1 with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
+ */
+mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const void *kv,
+                                   int64_t pool_rows, const int32_t *pages, int64_t num_pages,
+                                   const int32_t *indptr, const int32_t *last_page_len, int page_size,
+                                   int num_requests, int qlen, int heads, float scale, float kv_scale,
+                                   int num_splits, int split_tokens, void *o, float *lse,
+                                   unsigned int flags, void *stream);
+
+/*
  * mla_merge_splits -- LSE merge of split partials into the latent.
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,

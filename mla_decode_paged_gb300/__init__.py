@@ -65,6 +65,8 @@ def library() -> ctypes.CDLL:
                                       vp, vp, vp]
     lib.mla_decode_attend_ex.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32,
                                          vp, vp, ctypes.c_uint, vp]
+    lib.mla_decode_attend_paged.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
+                                            i32, i32, vp, vp, ctypes.c_uint, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.mla_merge_value_gate.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
@@ -72,7 +74,7 @@ def library() -> ctypes.CDLL:
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mla_kv_append.argtypes = [vp, i64, vp, i64, vp, i64, f32, vp, i64, vp]
-    for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
+    for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
                  "mla_device_status", "mla_choose_splits", "mla_kv_append"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -118,7 +120,7 @@ def _as_u8(kv: torch.Tensor) -> torch.Tensor:
 
 
 def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
-           o=None, lse=None, causal=False, stream=None):
+           o=None, lse=None, causal=False, page_size=1, last_page_len=None, stream=None):
     """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
     lse [num_splits, S, heads] f32)``.
 
@@ -127,6 +129,9 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     fp8 codes; ``pages``/``indptr``: int32; S = (len(indptr) - 1) * qlen.
     ``causal``: row tq of a request sees only its first L - qlen + tq + 1
     tokens (``mla_decode_attend_ex`` with ``MLA_ATTEND_CAUSAL``).
+    ``page_size`` > 1: block tables (``pages`` = block indices, ``indptr``
+    counts blocks, ``last_page_len`` int32 [R] rows used in each request's
+    last block; ``mla_decode_attend_paged``).
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
@@ -142,8 +147,12 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
         o = torch.empty((num_splits, S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((num_splits, S, heads), dtype=torch.float32, device=q.device)
-    st = library().mla_decode_attend_ex(
-        _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr), R, qlen,
+    if page_size > 1:
+        _need(last_page_len is not None and last_page_len.dtype == torch.int32 and last_page_len.numel() == R
+              and last_page_len.is_contiguous(), "page_size > 1 needs last_page_len int32 [R]")
+    st = library().mla_decode_attend_paged(
+        _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
+        _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
         heads, float(scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o), _ptr(lse),
         ATTEND_CAUSAL if causal else 0, ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_decode_attend")

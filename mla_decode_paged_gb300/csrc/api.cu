@@ -21,7 +21,8 @@ cudaError_t attend_mma_status(unsigned int *flags, bool clear);
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, bool causal, int grid, cudaStream_t st);
+                             float *lse, bool causal, int log2p, const int32_t *last_page_len, int grid,
+                             cudaStream_t st);
 cudaError_t attend_tc_status(unsigned int *flags, bool clear);
 cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
                          void *latent, float *lse_out, cudaStream_t st);
@@ -90,7 +91,23 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
                                 int num_requests, int qlen, int heads, float scale, float kv_scale,
                                 int num_splits, int split_tokens, void *o, float *lse, unsigned int flags,
                                 void *stream) {
+    return mla_decode_attend_paged(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, nullptr, 1,
+                                   num_requests, qlen, heads, scale, kv_scale, num_splits, split_tokens, o, lse,
+                                   flags, stream);
+}
+
+mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                   const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                                   const int32_t *last_page_len, int page_size, int num_requests, int qlen,
+                                   int heads, float scale, float kv_scale, int num_splits, int split_tokens,
+                                   void *o, float *lse, unsigned int flags, void *stream) {
     if (flags & ~MLA_ATTEND_CAUSAL) return fail(MLA_ERR_INVALID, "unknown flag bits");
+    int log2p = 0;
+    while ((1 << log2p) < page_size && log2p < 9) ++log2p;
+    if (page_size < 1 || page_size > 256 || (1 << log2p) != page_size)
+        return fail(MLA_ERR_INVALID, "page_size must be a power of two in 1..256");
+    if (page_size > 1 && (pool_rows % page_size != 0))
+        return fail(MLA_ERR_INVALID, "pool_rows must be a multiple of page_size");
     const bool causal = (flags & MLA_ATTEND_CAUSAL) != 0;
     if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
     if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
@@ -109,7 +126,10 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
         return fail(MLA_ERR_INVALID, "misaligned pointer (q, kv, o need 16 bytes)");
     if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
     if (pool_rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "pool_rows above 2^31 - 1");
+    if (page_size > 1 && (!last_page_len || !aligned(last_page_len, 4)))
+        return fail(MLA_ERR_INVALID, "page_size > 1 needs last_page_len (int32, 4-byte aligned)");
     if (causal && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "causal mask with the warp-MMA kernel");
+    if (page_size > 1 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "page_size > 1 with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_warp_mma()
                         ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
@@ -117,7 +137,7 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
                                                  split_tokens, o, lse, device_sms(), st)
                         : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                split_tokens, o, lse, causal, device_sms(), st);
+                                                split_tokens, o, lse, causal, log2p, last_page_len, device_sms(), st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }

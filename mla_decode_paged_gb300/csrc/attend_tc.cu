@@ -114,11 +114,20 @@ struct Params {
     int64_t num_pages;
     const int32_t *indptr;
     int R, qlen, heads, num_splits, split_tokens, row_groups, nq, causal;
+    int log2p;                          // blocks of 2^log2p rows (0: flat token rows)
+    const int32_t *last_page_len;       // rows used in each request's last block (log2p > 0)
     float sc_log2;
     float kv_scale;
     __nv_bfloat16 *o;
     float *lse;
 };
+
+// Tokens of request r (indptr already validated by the producers for any
+// request that reaches the softmax with tokens).
+__device__ __forceinline__ int request_tokens(const Params &P, int r) {
+    const int a = __ldg(P.indptr + r), b = __ldg(P.indptr + r + 1);
+    return (P.log2p == 0 || b == a) ? b - a : ((b - a - 1) << P.log2p) + __ldg(P.last_page_len + r);
+}
 
 template <int NQ>
 __device__ __forceinline__ Misc<NQ> &misc(uint8_t *sm) {
@@ -215,16 +224,20 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
     const bool has_op = op < C::Ops;
     const int g4 = op / 5, part = op % 5;
     TileIter<C::T> iter;
-    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
+    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, P.log2p,
+              P.last_page_len);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int tok = 4 * g4 + i;
             int r = -1;
             if (T.valid && has_op && tok < T.ntok) {
-                const int64_t p = __ldg(P.pages + (int64_t)T.base + T.tok0 + tok);
-                if (p < 0 || p >= P.pool_rows) flag(MLA_DEV_BAD_PAGE);
-                else r = (int)p;
+                // token j of the request: row pages[base + j / 2^log2p] * 2^log2p + j % 2^log2p
+                const int j = T.tok0 + tok;
+                const int64_t p = __ldg(P.pages + (int64_t)T.base + (j >> P.log2p));
+                const int64_t row = (p << P.log2p) + (j & ((1 << P.log2p) - 1));
+                if (p < 0 || row >= P.pool_rows) flag(MLA_DEV_BAD_PAGE);
+                else r = (int)row;
             }
             rows[i] = r;
         }
@@ -554,13 +567,13 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
                                    ? ((int64_t)M.k * S + (int64_t)M.r * P.qlen + rho / P.heads) * P.heads + rho % P.heads
                                    : -1;
                 if (CAUSAL) {   // L_r from indptr (validated by the producers: ntok > 0 here)
-                    const int len = __ldg(P.indptr + M.r + 1) - __ldg(P.indptr + M.r);
+                    const int len = request_tokens(P, M.r);
                     ms.vis[tid] = len - P.qlen + rho / P.heads + 1;
                 }
             }
             // vis[] is read below by every softmax thread in this same tile
             if (CAUSAL) {
-                vmin = __ldg(P.indptr + M.r + 1) - __ldg(P.indptr + M.r) - P.qlen + 1;
+                vmin = request_tokens(P, M.r) - P.qlen + 1;
                 named_sync(kSoftBar, kSoftThreads);
             }
         }
@@ -818,7 +831,8 @@ void attend_tc_shape(int rows, int *groups, int *nq) {
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, bool causal, int grid, cudaStream_t st) {
+                             float *lse, bool causal, int log2p, const int32_t *last_page_len, int grid,
+                             cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap ml, mr;
@@ -846,6 +860,8 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
     P.num_splits = num_splits;
     P.split_tokens = split_tokens;
     P.causal = causal ? 1 : 0;
+    P.log2p = log2p;
+    P.last_page_len = last_page_len;
     P.sc_log2 = scale * kv_scale * 1.4426950408889634f;
     P.kv_scale = kv_scale;
     P.o = static_cast<__nv_bfloat16 *>(o);

@@ -210,11 +210,14 @@ __device__ __forceinline__ void split_range(int len, int n, int k, int *start, i
     *count = b + (k < m ? 1 : 0);
 }
 
-// Length of request r from indptr, validated against num_pages: a
-// decreasing or out-of-range entry flags MLA_DEV_BAD_INDPTR and yields an
-// empty request (the kernels then never index pages with it).
-__device__ __forceinline__ int request_len(const int32_t *indptr, int r, int64_t num_pages,
-                                           int *base) {
+// Length (tokens) of request r from indptr, validated against num_pages:
+// a decreasing or out-of-range entry flags MLA_DEV_BAD_INDPTR and yields an
+// empty request (the kernels then never index pages with it).  With blocks
+// of 2^log2p rows, indptr counts blocks and the last block holds
+// last_page_len[r] (1..2^log2p) rows; a value outside that range is flagged
+// the same way.
+__device__ __forceinline__ int request_len(const int32_t *indptr, int r, int64_t num_pages, int *base,
+                                           int log2p = 0, const int32_t *last_page_len = nullptr) {
     int a = __ldg(indptr + r), b = __ldg(indptr + r + 1);
     if (a < 0 || b < a || (int64_t)b > num_pages) {
         flag(MLA_DEV_BAD_INDPTR);
@@ -222,7 +225,13 @@ __device__ __forceinline__ int request_len(const int32_t *indptr, int r, int64_t
         return 0;
     }
     *base = a;
-    return b - a;
+    if (log2p == 0 || b == a) return b - a;
+    const int last = __ldg(last_page_len + r);
+    if (last < 1 || last > (1 << log2p)) {
+        flag(MLA_DEV_BAD_INDPTR);
+        return 0;
+    }
+    return ((b - a - 1) << log2p) + last;
 }
 
 // Address of the KV row that token slot i (an index into pages) names.  A
@@ -249,14 +258,18 @@ __device__ __forceinline__ const uint8_t *kv_row(const uint8_t *kv, const int32_
 // non-decreasing u order.  Every lane of the warp must call find() together.
 struct UnitCursor {
     const int32_t *indptr;
+    const int32_t *last_page_len;   // block tables only
     int64_t num_pages;
-    int R, num_splits, split_tokens;
+    int R, num_splits, split_tokens, log2p;
     int r_base;
     long long cum_base;
     int n, incl, len, base;
 
-    __device__ void init(const int32_t *ip, int r_count, int64_t pages_len, int ns, int st, int lane) {
+    __device__ void init(const int32_t *ip, int r_count, int64_t pages_len, int ns, int st, int lane,
+                         int lp = 0, const int32_t *last = nullptr) {
         indptr = ip;
+        last_page_len = last;
+        log2p = lp;
         R = r_count;
         num_pages = pages_len;
         num_splits = ns;
@@ -269,7 +282,7 @@ struct UnitCursor {
     __device__ void load(int lane) {
         const int r = r_base + lane;
         if (r < R) {
-            len = request_len(indptr, r, num_pages, &base);
+            len = request_len(indptr, r, num_pages, &base, log2p, last_page_len);
             n = split_count(len, num_splits, split_tokens);
         } else {
             len = 0;
@@ -327,8 +340,8 @@ struct TileIter {
 
     int row_groups;
     __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
-                         int groups, int lane) {
-        cur.init(indptr, R, num_pages, num_splits, split_tokens, lane);
+                         int groups, int lane, int log2p = 0, const int32_t *last_page_len = nullptr) {
+        cur.init(indptr, R, num_pages, num_splits, split_tokens, lane, log2p, last_page_len);
         row_groups = groups;
         u = (long long)blockIdx.x - gridDim.x;
         have_unit = false;

@@ -133,3 +133,35 @@ def test_choose_splits_plan_is_valid(R, qlen, H, max_len, total):
     lens = [max_len] + [max(0, (total - max_len) // max(1, R - 1))] * (R - 1)
     ns2, st2 = mla.choose_splits(R, qlen, H, sm_count=152, lengths=lens)
     assert 1 <= ns2 <= 256 and -(-max_len // st2) <= ns2
+
+
+def _attend_paged(lib, page_size, last=P16, flags=0, **kw):
+    a = dict(q=P16, q_row_stride=12 * 576, kv=P16, pool_rows=128, pages=P16, num_pages=10, indptr=P16,
+             R=2, qlen=1, heads=12, scale=0.1, kv_scale=1.0, num_splits=4, split_tokens=16, o=P16, lse=P16,
+             stream=NULL)
+    a.update(kw)
+    return lib.mla_decode_attend_paged(a["q"], a["q_row_stride"], a["kv"], a["pool_rows"], a["pages"],
+                                       a["num_pages"], a["indptr"], last, page_size, a["R"], a["qlen"], a["heads"],
+                                       a["scale"], a["kv_scale"], a["num_splits"], a["split_tokens"], a["o"],
+                                       a["lse"], flags, a["stream"])
+
+
+@pytest.mark.parametrize("page_size,kw,msg", [
+    (0, {}, b"page_size"), (3, {}, b"page_size"), (512, {}, b"page_size"), (24, {}, b"page_size"),
+    (16, dict(pool_rows=100), b"multiple of page_size"),
+])
+def test_attend_paged_rejects_bad_page_arguments(lib, page_size, kw, msg):
+    assert _attend_paged(lib, page_size, **kw) == mla.MLA_ERR_INVALID
+    assert msg in lib.mla_last_error()
+
+
+def test_attend_paged_needs_last_page_len(lib):
+    assert _attend_paged(lib, 16, last=NULL) == mla.MLA_ERR_INVALID
+    assert b"last_page_len" in lib.mla_last_error()
+    assert _attend_paged(lib, 16, last=ctypes.c_void_p((1 << 20) + 2)) == mla.MLA_ERR_INVALID
+
+
+def test_attend_paged_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
+    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
+    assert _attend_paged(lib, 16) == mla.MLA_ERR_UNSUPPORTED
+    assert b"page_size" in lib.mla_last_error()

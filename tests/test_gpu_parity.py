@@ -350,3 +350,78 @@ def test_causal_full_size_sampled(idx):
     assert_bf16_close(out[rows], rout[rows], "causal out (sampled)")
     assert torch.isfinite(latent).all() and torch.isfinite(out).all()
     assert mla.device_status() == 0
+
+
+# ------------------------------------------------------- block-table caches
+
+def _to_blocks(inp, device):
+    out = _to(inp, device)
+    out.extra["page_size"] = inp.extra["page_size"]
+    out.extra["last_page_len"] = inp.extra["last_page_len"].to(device)
+    return out
+
+
+@pytest.mark.parametrize("P,idx,lengths", [(2, 4, [0, 5, 200, 0, 333]), (16, 1, [1, 17, 128, 129, 300, 1000]),
+                                           (64, 2, [257, 64, 700]), (16, 3, [300, 129])])
+@pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (3, 7)])
+def test_block_table_small_workloads_match_oracle(P, idx, lengths, plan):
+    inp_cpu = W.make_block_inputs(idx, "cpu", page_size=P, lengths=lengths)
+    inp = _to_blocks(inp_cpu, DEV)
+    last = inp.extra["last_page_len"]
+    ns, st = plan
+    o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=inp.heads,
+                        qlen=inp.qlen, page_size=P, last_page_len=last)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    a = oracle_args(inp_cpu)
+    lp = i32(inp_cpu.extra["last_page_len"])
+    ro, rl = O.attend_splits(**a, num_splits=ns, split_tokens=st, page_size=P, last_page_len=lp)
+    assert_lse_close(lse, rl, "block-table partial lse")
+    assert_bf16_close(o, ro, "block-table partial o", mask=np.isfinite(rl))
+    rlat, rlse = O.attend(**a, page_size=P, last_page_len=lp)
+    assert_lse_close(lse_m, rlse, "block-table merged lse")
+    assert_bf16_close(latent, rlat, "block-table latent")
+    assert mla.device_status() == 0
+
+
+def test_block_table_causal_matches_oracle():
+    inp_cpu = W.make_block_inputs(2, "cpu", page_size=16, lengths=[2, 3, 257, 700])
+    inp = _to_blocks(inp_cpu, DEV)
+    o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 4, 64, heads=inp.heads,
+                        qlen=inp.qlen, page_size=16, last_page_len=inp.extra["last_page_len"], causal=True)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    rlat, rlse = O.attend(**oracle_args(inp_cpu), page_size=16, last_page_len=i32(inp_cpu.extra["last_page_len"]),
+                          causal=True)
+    assert_lse_close(lse_m, rlse, "block-table causal lse")
+    assert_bf16_close(latent, rlat, "block-table causal latent")
+    assert mla.device_status() == 0
+
+
+def test_block_table_full_decode_batch_sampled():
+    inp = W.make_block_inputs(1, DEV, page_size=16)
+    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
+    last = inp.extra["last_page_len"]
+    o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=inp.heads,
+                        page_size=16, last_page_len=last)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    lens = i32(inp.lengths)
+    reqs = _sample_requests(lens, seed=31)
+    a = dict(q_bits=bf16_bits(inp.q), kv_codes=u8(inp.kv), pages=i32(inp.pages), indptr=i32(inp.indptr),
+             scale=inp.scale, kv_scale=inp.kv_scale, heads=inp.heads, qlen=inp.qlen)
+    rlat, rlse = O.attend(**a, requests=reqs, page_size=16, last_page_len=i32(last))
+    assert_lse_close(lse_m[reqs], rlse[reqs], "block-table lse (sampled)")
+    assert_bf16_close(latent[reqs], rlat[reqs], "block-table latent (sampled)")
+    assert torch.isfinite(latent).all()
+    assert mla.device_status() == 0
+
+
+def test_block_table_bad_last_page_len_is_flagged_not_faulted():
+    inp = _to_blocks(W.make_block_inputs(1, "cpu", page_size=16, lengths=[40, 300]), DEV)
+    last = inp.extra["last_page_len"].clone()
+    last[1] = 17                                         # more rows than a block holds
+    mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 2, 64, heads=inp.heads,
+               page_size=16, last_page_len=last)
+    assert mla.device_status() & mla.DEV_BAD_INDPTR
+    assert mla.device_status() == 0
