@@ -178,8 +178,18 @@ def dequant(codes, kv_scale: float) -> np.ndarray:
     return e4m3fn_to_f64(codes) * float(kv_scale)
 
 
+def query_rows(q, t0: int, t1: int, heads: int, q_fp8: bool = False) -> np.ndarray:
+    """Query rows t0..t1-1, real heads only, as float64 [(t1-t0)*heads, 576]:
+    bf16 bits (the pages' q), or with ``q_fp8`` e4m3 codes (the DCP8 input
+    ``q8``; its ``_q_scale`` multiplies the softmax scale, the caller folds
+    it into ``scale``)."""
+    blk = np.asarray(q)[t0:t1, :heads, :]
+    vals = e4m3fn_to_f64(blk) if q_fp8 else bf16_to_f64(blk)
+    return vals.reshape((t1 - t0) * heads, D_QK)
+
+
 def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-           requests=None, return_p=False, causal=False, page_size=1, last_page_len=None):
+           requests=None, return_p=False, causal=False, page_size=1, last_page_len=None, q_fp8=False):
     """The unsplit attention: latent [S, H, 512] and LSE [S, H].
 
     ``q_bits``: uint16 bf16 bits [S, H_pad, 576]; only heads < ``heads`` are
@@ -188,6 +198,7 @@ def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     left NaN), so that full-size workloads can be checked on a sample.
     ``causal``: apply :func:`causal_visible` to each request's rows.
     ``page_size`` / ``last_page_len``: block tables (:func:`request_rows`).
+    ``q_fp8``: ``q_bits`` holds e4m3 codes (:func:`query_rows`).
     """
     q = np.asarray(q_bits)
     R = len(indptr) - 1
@@ -197,7 +208,7 @@ def attend(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     ps = {}
     for r in (range(R) if requests is None else requests):
         K = dequant(gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len), kv_scale)
-        rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
+        rows = query_rows(q, r * qlen, (r + 1) * qlen, heads, q_fp8)
         vis = causal_visible(K.shape[0], qlen, heads) if causal else None
         lat, l, p = attend_rows(rows, K, scale, vis)
         latent[r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)
@@ -236,7 +247,8 @@ def split_plan(L: int, num_splits: int, split_tokens: int):
 
 
 def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
-                  num_splits, split_tokens, requests=None, causal=False, page_size=1, last_page_len=None):
+                  num_splits, split_tokens, requests=None, causal=False, page_size=1, last_page_len=None,
+                  q_fp8=False):
     """Per-split partials: o [num_splits, S, H, 512] (float64) and lse
     [num_splits, S, H]; each used split is the attention restricted to its
     token range (``m1c_inputs``: new partials o [splits, S, 12, 512], LSE
@@ -254,7 +266,7 @@ def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
     for r in (range(R) if requests is None else requests):
         lse[:, r * qlen:(r + 1) * qlen] = -np.inf
         K = dequant(gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len), kv_scale)
-        rows = bf16_to_f64(q[r * qlen:(r + 1) * qlen, :heads, :]).reshape(qlen * heads, D_QK)
+        rows = query_rows(q, r * qlen, (r + 1) * qlen, heads, q_fp8)
         vis = causal_visible(K.shape[0], qlen, heads) if causal else np.full(qlen * heads, K.shape[0])
         for k, (a, b) in enumerate(split_plan(K.shape[0], num_splits, split_tokens)):
             lat, l, _ = attend_rows(rows, K[a:b], scale, vis - a)

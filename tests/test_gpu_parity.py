@@ -425,3 +425,26 @@ def test_block_table_bad_last_page_len_is_flagged_not_faulted():
                page_size=16, last_page_len=last)
     assert mla.device_status() & mla.DEV_BAD_INDPTR
     assert mla.device_status() == 0
+
+
+@pytest.mark.parametrize("ranks", [2, 4])
+def test_second_level_combine_of_sharded_partials(ranks):
+    """Partials computed separately over each decode-context-parallel shard
+    (token i of a request on rank i % ranks), concatenated along the split
+    axis and merged by mla_merge_splits: the full attention."""
+    from tests.test_oracle import _shard_by_slot
+    inp_cpu = W.make_inputs(4, "cpu", lengths=[0, 5, 200, 333, 1, 700])
+    inp = _to(inp_cpu, DEV)
+    a = oracle_args(inp_cpu)
+    os_, ls_ = [], []
+    for k, (pg, ip) in enumerate(_shard_by_slot(a["pages"], a["indptr"], ranks)):
+        o, lse = mla.attend(inp.q, inp.kv, torch.from_numpy(pg).to(DEV), torch.from_numpy(ip).to(DEV), inp.scale,
+                            inp.kv_scale, 2 + k, 64, heads=inp.heads, qlen=inp.qlen)
+        os_.append(o)
+        ls_.append(lse)
+    latent, lse_m = mla.merge(torch.cat(os_).contiguous(), torch.cat(ls_).contiguous())
+    torch.cuda.synchronize()
+    rlat, rlse = O.attend(**a)
+    assert_lse_close(lse_m, rlse, "combined lse")
+    assert_bf16_close(latent, rlat, "combined latent")
+    assert mla.device_status() == 0

@@ -476,3 +476,59 @@ def test_block_table_attention_equals_flat_page_list(P):
     o, ls = O.attend_splits(**a, num_splits=5, split_tokens=50, page_size=P, last_page_len=last)
     o1, ls1 = O.attend_splits(**flat, num_splits=5, split_tokens=50)
     assert np.array_equal(ls, ls1) and np.array_equal(np.nan_to_num(o, nan=7.0), np.nan_to_num(o1, nan=7.0))
+
+
+def _shard_by_slot(pages, indptr, ranks):
+    """Decode-context-parallel sharding: token i of a request goes to rank
+    i % ranks; returns each rank's (pages, indptr)."""
+    out = []
+    for k in range(ranks):
+        pg, ip = [], [0]
+        for r in range(len(indptr) - 1):
+            own = pages[indptr[r]:indptr[r + 1]][k::ranks]
+            pg.extend(own.tolist())
+            ip.append(ip[-1] + len(own))
+        out.append((np.array(pg, np.int32), np.array(ip, np.int32)))
+    return out
+
+
+@pytest.mark.parametrize("ranks", [2, 3])
+def test_combine_of_sharded_partials_equals_full_attention(ranks):
+    """The second-level LSE combine (``post``: the DCP combine of per-rank
+    partials) is the same merge: attention over each rank's slice of the
+    context, stacked as splits and merged, equals attention over it all."""
+    inp = W.make_inputs(4, "cpu", lengths=[0, 5, 200, 333, 1])
+    a = oracle_args(inp)
+    lat, lse = O.attend(**a)
+    parts_o, parts_l = [], []
+    for pg, ip in _shard_by_slot(a["pages"], a["indptr"], ranks):
+        o, l = O.attend_splits(**dict(a, pages=pg, indptr=ip), num_splits=2, split_tokens=64)
+        parts_o.append(o)
+        parts_l.append(l)
+    mlat, mlse = O.merge(np.concatenate(parts_o), np.concatenate(parts_l))
+    assert np.allclose(mlat, lat, atol=1e-12, rtol=1e-12)
+    assert np.array_equal(np.isneginf(mlse), np.isneginf(lse))
+    f = np.isfinite(lse)
+    assert np.allclose(mlse[f], lse[f], atol=1e-12)
+
+
+# ---------------------------------------------------------------- fp8 query
+
+def test_fp8_query_equals_the_bf16_query_of_the_same_values():
+    """An e4m3 query is exactly representable in bf16: attention over q8
+    with scale s equals attention over bf16(q8 values) with scale s, and a
+    q_scale folded into the scale equals scaling the query values."""
+    inp = W.make_inputs(4, "cpu", lengths=[0, 5, 200, 33])
+    a = oracle_args(inp)
+    q8 = (inp.q.float() * 7).to(torch.float8_e4m3fn)          # some codes saturate, fine
+    as_bf16 = q8.float().to(torch.bfloat16)
+    assert torch.equal(as_bf16.float(), q8.float())               # exact widening
+    lat8, lse8 = O.attend(**dict(a, q_bits=u8(q8.view(torch.uint8))), q_fp8=True)
+    latb, lseb = O.attend(**dict(a, q_bits=bf16_bits(as_bf16)))
+    assert np.array_equal(lat8, latb) and np.array_equal(lse8, lseb)
+    qs = 0.25
+    lat_s, lse_s = O.attend(**dict(a, q_bits=u8(q8.view(torch.uint8)), scale=a["scale"] * qs), q_fp8=True)
+    scaled = (q8.float() * qs).to(torch.bfloat16)                 # exact: power-of-two scale
+    lat_r, lse_r = O.attend(**dict(a, q_bits=bf16_bits(scaled)))
+    assert np.allclose(lat_s, lat_r, atol=1e-12) and np.allclose(np.nan_to_num(lse_s, neginf=0),
+                                                                 np.nan_to_num(lse_r, neginf=0), atol=1e-12)
