@@ -106,6 +106,7 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
 
 /* Flags of mla_decode_attend_ex. */
 #define MLA_ATTEND_CAUSAL 1u   /* causal mask within a request (qlen > 1)    */
+#define MLA_ATTEND_Q_FP8 2u    /* q holds fp8 e4m3 codes (DCP8's q8)         */
 
 /*
  * mla_decode_attend_ex -- mla_decode_attend with option flags.
@@ -118,9 +119,14 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
  * none, lse = -inf and o is 0 (so a row that sees no token at all merges
  * to latent 0, LSE -inf).  flags = 0 is exactly mla_decode_attend.
  *
+ * MLA_ATTEND_Q_FP8: q holds e4m3 codes, one byte per element (the pages'
+ * decode-context-parallel input q8, whose _q_scale multiplies every score:
+ * pass scale * q_scale as scale); q_row_stride counts bytes and must be a
+ * multiple of 16.  The score is scale * <e4m3(q), K>.
+ *
  * Arguments as mla_decode_attend.  Unknown flag bits: MLA_ERR_INVALID.
- * MLA_ATTEND_CAUSAL with the warp-MMA kernel (environment
- * MLA_ATTEND_KERNEL=mma): MLA_ERR_UNSUPPORTED.
+ * MLA_ATTEND_CAUSAL or MLA_ATTEND_Q_FP8 with the warp-MMA kernel
+ * (environment MLA_ATTEND_KERNEL=mma): MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void *kv,
                                 int64_t pool_rows, const int32_t *pages, int64_t num_pages,

@@ -26,7 +26,7 @@ from . import build as _build
 
 D_QK, D_LATENT, D_V = 576, 512, 128
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
-ATTEND_CAUSAL = 1
+ATTEND_CAUSAL, ATTEND_Q_FP8 = 1, 2
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
 
 __all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "debug_gather",
@@ -120,7 +120,7 @@ def _as_u8(kv: torch.Tensor) -> torch.Tensor:
 
 
 def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
-           o=None, lse=None, causal=False, page_size=1, last_page_len=None, stream=None):
+           o=None, lse=None, causal=False, page_size=1, last_page_len=None, q_scale=1.0, stream=None):
     """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
     lse [num_splits, S, heads] f32)``.
 
@@ -132,12 +132,18 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     ``page_size`` > 1: block tables (``pages`` = block indices, ``indptr``
     counts blocks, ``last_page_len`` int32 [R] rows used in each request's
     last block; ``mla_decode_attend_paged``).
+    A ``q`` of dtype float8_e4m3fn / uint8 is an fp8 query (codes); its
+    ``q_scale`` multiplies the softmax scale (``MLA_ATTEND_Q_FP8``).
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
     R = indptr.numel() - 1
     S = R * qlen
-    _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == D_QK, "q must be bf16 [S, H, 576]")
+    q8 = q.dtype in (torch.float8_e4m3fn, torch.uint8)
+    if q.dtype == torch.float8_e4m3fn:
+        q = q.view(torch.uint8)
+    _need((q8 or q.dtype == torch.bfloat16) and q.dim() == 3 and q.shape[2] == D_QK,
+          "q must be bf16 or fp8 e4m3 [S, H, 576]")
     _need(q.stride(2) == 1 and q.stride(1) == D_QK, "q rows must have contiguous [H, 576] heads")
     _need(q.shape[0] == S and heads <= q.shape[1], "q shape does not match indptr / qlen / heads")
     _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
@@ -153,8 +159,8 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     st = library().mla_decode_attend_paged(
         _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
         _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
-        heads, float(scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o), _ptr(lse),
-        ATTEND_CAUSAL if causal else 0, ctypes.c_void_p(_stream(stream)))
+        heads, float(scale) * float(q_scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o),
+        _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_decode_attend")
     return o, lse
 

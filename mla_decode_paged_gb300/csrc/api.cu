@@ -21,8 +21,8 @@ cudaError_t attend_mma_status(unsigned int *flags, bool clear);
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, bool causal, int log2p, const int32_t *last_page_len, int grid,
-                             cudaStream_t st);
+                             float *lse, bool causal, int log2p, const int32_t *last_page_len, bool q8,
+                             int grid, cudaStream_t st);
 cudaError_t attend_tc_status(unsigned int *flags, bool clear);
 cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
                          void *latent, float *lse_out, cudaStream_t st);
@@ -101,7 +101,8 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                    const int32_t *last_page_len, int page_size, int num_requests, int qlen,
                                    int heads, float scale, float kv_scale, int num_splits, int split_tokens,
                                    void *o, float *lse, unsigned int flags, void *stream) {
-    if (flags & ~MLA_ATTEND_CAUSAL) return fail(MLA_ERR_INVALID, "unknown flag bits");
+    if (flags & ~(MLA_ATTEND_CAUSAL | MLA_ATTEND_Q_FP8)) return fail(MLA_ERR_INVALID, "unknown flag bits");
+    const bool q8 = (flags & MLA_ATTEND_Q_FP8) != 0;
     int log2p = 0;
     while ((1 << log2p) < page_size && log2p < 9) ++log2p;
     if (page_size < 1 || page_size > 256 || (1 << log2p) != page_size)
@@ -114,8 +115,9 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
     if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
     if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return fail(MLA_ERR_INVALID, "num_splits outside 1..256");
     if (split_tokens < 1) return fail(MLA_ERR_INVALID, "split_tokens < 1");
-    if (q_row_stride < (int64_t)heads * MLA_D_QK || q_row_stride % 8 != 0)
-        return fail(MLA_ERR_INVALID, "q_row_stride must be >= heads*576 and a multiple of 8");
+    if (q_row_stride < (int64_t)heads * MLA_D_QK || q_row_stride % (q8 ? 16 : 8) != 0)
+        return fail(MLA_ERR_INVALID, q8 ? "q_row_stride must be >= heads*576 and a multiple of 16 (fp8 q)"
+                                        : "q_row_stride must be >= heads*576 and a multiple of 8");
     if (pool_rows < 0 || num_pages < 0) return fail(MLA_ERR_INVALID, "negative pool_rows / num_pages");
     if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return fail(MLA_ERR_INVALID, "non-finite scale");
     if (num_requests == 0) return MLA_OK;
@@ -130,6 +132,7 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
         return fail(MLA_ERR_INVALID, "page_size > 1 needs last_page_len (int32, 4-byte aligned)");
     if (causal && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "causal mask with the warp-MMA kernel");
     if (page_size > 1 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "page_size > 1 with the warp-MMA kernel");
+    if (q8 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "fp8 query with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_warp_mma()
                         ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
@@ -137,7 +140,8 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                                  split_tokens, o, lse, device_sms(), st)
                         : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                split_tokens, o, lse, causal, log2p, last_page_len, device_sms(), st);
+                                                split_tokens, o, lse, causal, log2p, last_page_len, q8, device_sms(),
+                                                st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }

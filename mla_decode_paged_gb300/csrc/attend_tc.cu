@@ -115,6 +115,7 @@ struct Params {
     const int32_t *indptr;
     int R, qlen, heads, num_splits, split_tokens, row_groups, nq, causal;
     int log2p;                          // blocks of 2^log2p rows (0: flat token rows)
+    int q8;                             // q holds e4m3 codes (row stride in bytes)
     const int32_t *last_page_len;       // rows used in each request's last block (log2p > 0)
     float sc_log2;
     float kv_scale;
@@ -382,6 +383,44 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
 
 // ------------------------------------------------------------------ softmax
 
+// An fp8 query (e4m3 codes, the q_scale folded into the softmax scale):
+// row n of Q' holds the codes as they are, row NQ + n (the lo term) zeros,
+// c[n] = scale * kv_scale * log2(e).  Run by the 8 softmax warps; a warp
+// copies a 576-byte row as 36 16-byte chunks into the swizzled layouts.
+template <int NQ>
+__device__ __noinline__ void prep_rows_q8(const Params &P, uint8_t *sm, int req, int grp) {
+    using C = Cfg<NQ>;
+    Misc<NQ> &ms = misc<NQ>(sm);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rows_total = P.qlen * P.heads;
+    for (int n = warp; n < NQ; n += kSoftWarps) {
+        const int rho = grp * NQ + n;
+        const bool valid = rho < rows_total;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(P.q);
+        if (valid) {
+            const int tq = rho / P.heads, h = rho % P.heads;
+            src += ((int64_t)req * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK;
+        }
+        for (int ch = lane; ch < MLA_D_QK / 16; ch += 32) {
+            const uint4 v = valid ? __ldg(reinterpret_cast<const uint4 *>(src) + ch) : make_uint4(0, 0, 0, 0);
+            const int d = ch * 16;
+            uint32_t off_hi, off_lo;
+            if (d < 512) {
+                const uint32_t blk = C::OffQ + (d >> 7) * C::QLatBlock;
+                off_hi = blk + (n >> 3) * 1024 + tc::sw128(n, d & 127);
+                off_lo = blk + ((NQ + n) >> 3) * 1024 + tc::sw128(NQ + n, d & 127);
+            } else {
+                const uint32_t blk = C::OffQ + C::QRope;
+                off_hi = blk + (n >> 3) * 512 + tc::sw64(n, d - 512);
+                off_lo = blk + ((NQ + n) >> 3) * 512 + tc::sw64(NQ + n, d - 512);
+            }
+            *reinterpret_cast<uint4 *>(sm + off_hi) = v;
+            *reinterpret_cast<uint4 *>(sm + off_lo) = make_uint4(0, 0, 0, 0);
+        }
+        if (lane == 0) ms.c[n] = valid ? P.sc_log2 : 0.f;
+    }
+}
+
 // The query rows of tile T's request and row group as the B operand Q':
 // row n = q_n * 2^e_n rounded to e4m3 (hi), row NQ + n = 16 * (q_n * 2^e_n
 // - hi) rounded to e4m3 (lo), in the K-major 128B / 64B swizzled layouts;
@@ -392,6 +431,9 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_total = P.qlen * P.heads;
+    if (P.q8) {
+        prep_rows_q8<NQ>(P, sm, req, grp);
+    } else {
     constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6 rows per warp, all loads in flight at once
     {
         constexpr int i0 = 0;
@@ -469,6 +511,7 @@ __device__ void prep_query(const Params &P, uint8_t *sm, int req, int grp) {
                 *reinterpret_cast<uint2 *>(sm + off_lo) = make_uint2(lo[0], lo[1]);
             }
         }
+    }
     }
     tc::fence_async_smem();   // generic-proxy writes -> tensor-core reads
     named_sync(kSoftBar, kSoftThreads);
@@ -831,8 +874,8 @@ void attend_tc_shape(int rows, int *groups, int *nq) {
 cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
-                             float *lse, bool causal, int log2p, const int32_t *last_page_len, int grid,
-                             cudaStream_t st) {
+                             float *lse, bool causal, int log2p, const int32_t *last_page_len, bool q8,
+                             int grid, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap ml, mr;
@@ -861,6 +904,7 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
     P.split_tokens = split_tokens;
     P.causal = causal ? 1 : 0;
     P.log2p = log2p;
+    P.q8 = q8 ? 1 : 0;
     P.last_page_len = last_page_len;
     P.sc_log2 = scale * kv_scale * 1.4426950408889634f;
     P.kv_scale = kv_scale;

@@ -90,7 +90,8 @@ def _attend_ex(lib, flags, **kw):
 
 
 def test_attend_ex_rejects_unknown_flags_and_checks_like_attend(lib):
-    assert _attend_ex(lib, 2) == mla.MLA_ERR_INVALID
+    # every case below must fail host validation: the pointers are fake
+    assert _attend_ex(lib, 4) == mla.MLA_ERR_INVALID
     assert b"flag" in lib.mla_last_error()
     assert _attend_ex(lib, 0x80000000) == mla.MLA_ERR_INVALID
     assert _attend_ex(lib, mla.ATTEND_CAUSAL, qlen=0) == mla.MLA_ERR_INVALID
@@ -165,3 +166,13 @@ def test_attend_paged_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
     monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
     assert _attend_paged(lib, 16) == mla.MLA_ERR_UNSUPPORTED
     assert b"page_size" in lib.mla_last_error()
+
+
+def test_fp8_query_flag_checks(lib, monkeypatch):
+    # fp8 rows: the stride counts bytes and must be a multiple of 16
+    assert _attend_ex(lib, mla.ATTEND_Q_FP8, q_row_stride=12 * 576 + 8) == mla.MLA_ERR_INVALID
+    assert b"multiple of 16" in lib.mla_last_error()
+    assert _attend_ex(lib, mla.ATTEND_Q_FP8 | 4) == mla.MLA_ERR_INVALID
+    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
+    assert _attend_ex(lib, mla.ATTEND_Q_FP8) == mla.MLA_ERR_UNSUPPORTED
+    assert b"fp8 query" in lib.mla_last_error()

@@ -448,3 +448,52 @@ def test_second_level_combine_of_sharded_partials(ranks):
     assert_lse_close(lse_m, rlse, "combined lse")
     assert_bf16_close(latent, rlat, "combined latent")
     assert mla.device_status() == 0
+
+
+# ------------------------------------------------------------ fp8 query
+
+def _q8(inp_cpu, gain=4.0):
+    """An fp8 query of the workload's shape (codes from q * gain, NaN pad heads kept)."""
+    return (inp_cpu.q.float() * gain).to(torch.float8_e4m3fn)
+
+
+@pytest.mark.parametrize("idx,lengths", [(1, [1, 17, 128, 129, 300, 1000]), (2, [257, 64, 700]), (3, [300, 129]),
+                                         (4, [0, 5, 200, 0, 333])])
+@pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (3, 7)])
+def test_fp8_query_small_workloads_match_oracle(idx, lengths, plan):
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    q8 = _q8(inp_cpu)
+    q_scale = 0.25
+    ns, st = plan
+    o, lse = mla.attend(q8.to(DEV), inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st,
+                        heads=inp.heads, qlen=inp.qlen, q_scale=q_scale)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    a = dict(oracle_args(inp_cpu), q_bits=u8(q8.view(torch.uint8)), scale=inp.scale * q_scale)
+    ro, rl = O.attend_splits(**a, num_splits=ns, split_tokens=st, q_fp8=True)
+    assert_lse_close(lse, rl, "fp8-q partial lse")
+    assert_bf16_close(o, ro, "fp8-q partial o", mask=np.isfinite(rl))
+    rlat, rlse = O.attend(**a, q_fp8=True)
+    assert_lse_close(lse_m, rlse, "fp8-q merged lse")
+    assert_bf16_close(latent, rlat, "fp8-q latent")
+    assert mla.device_status() == 0
+
+
+def test_fp8_query_full_size_sampled():
+    inp = W.make_inputs(2, DEV)
+    q8 = (inp.q.float() * 4).to(torch.float8_e4m3fn)
+    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
+    o, lse = mla.attend(q8, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=inp.heads,
+                        qlen=inp.qlen, q_scale=0.25)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    lens = i32(inp.lengths)
+    reqs = _sample_requests(lens, seed=41)
+    a = dict(q_bits=u8(q8.view(torch.uint8)), kv_codes=u8(inp.kv), pages=i32(inp.pages), indptr=i32(inp.indptr),
+             scale=inp.scale * 0.25, kv_scale=inp.kv_scale, heads=inp.heads, qlen=inp.qlen)
+    rlat, rlse = O.attend(**a, requests=reqs, q_fp8=True)
+    rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
+    assert_lse_close(lse_m[rows], rlse[rows], "fp8-q lse (sampled)")
+    assert_bf16_close(latent[rows], rlat[rows], "fp8-q latent (sampled)")
+    assert mla.device_status() == 0
