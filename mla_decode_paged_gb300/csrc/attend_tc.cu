@@ -216,7 +216,9 @@ __device__ __forceinline__ void colsum(float *v, int lane, int &base) {
 
 // ------------------------------------------------------------------ producers
 
-template <int NQ>
+// PAGED compiles in block-table addressing (a separate instantiation: the
+// flat-row path keeps its plain page lookup).
+template <int NQ, bool PAGED>
 __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtensorMap *mrope, uint8_t *sm) {
     using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
@@ -224,21 +226,30 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
     const int op = pw + kProdWarps * lane;  // ops dealt round-robin over the producer warps
     const bool has_op = op < C::Ops;
     const int g4 = op / 5, part = op % 5;
-    TileIter<C::T> iter;
-    iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, P.log2p,
-              P.last_page_len);
+    TileIter<C::T, PAGED> iter;
+    if (PAGED)
+        iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, P.log2p,
+                  P.last_page_len);
+    else
+        iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int tok = 4 * g4 + i;
             int r = -1;
             if (T.valid && has_op && tok < T.ntok) {
-                // token j of the request: row pages[base + j / 2^log2p] * 2^log2p + j % 2^log2p
-                const int j = T.tok0 + tok;
-                const int64_t p = __ldg(P.pages + (int64_t)T.base + (j >> P.log2p));
-                const int64_t row = (p << P.log2p) + (j & ((1 << P.log2p) - 1));
-                if (p < 0 || row >= P.pool_rows) flag(MLA_DEV_BAD_PAGE);
-                else r = (int)row;
+                if (PAGED) {
+                    // token j of the request: row pages[base + j / 2^log2p] * 2^log2p + j % 2^log2p
+                    const int j = T.tok0 + tok;
+                    const int64_t p = __ldg(P.pages + (int64_t)T.base + (j >> P.log2p));
+                    const int64_t row = (p << P.log2p) + (j & ((1 << P.log2p) - 1));
+                    if (p < 0 || row >= P.pool_rows) flag(MLA_DEV_BAD_PAGE);
+                    else r = (int)row;
+                } else {
+                    const int64_t p = __ldg(P.pages + (int64_t)T.base + T.tok0 + tok);
+                    if (p < 0 || p >= P.pool_rows) flag(MLA_DEV_BAD_PAGE);
+                    else r = (int)p;
+                }
             }
             rows[i] = r;
         }
@@ -388,7 +399,7 @@ __device__ void mma_issuer(const Params &P, uint8_t *sm) {
 // c[n] = scale * kv_scale * log2(e).  Run by the 8 softmax warps; a warp
 // copies a 576-byte row as 36 16-byte chunks into the swizzled layouts.
 template <int NQ>
-__device__ __noinline__ void prep_rows_q8(const Params &P, uint8_t *sm, int req, int grp) {
+__device__ void prep_rows_q8(const Params &P, uint8_t *sm, int req, int grp) {
     using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -779,7 +790,7 @@ __device__ void softmax(const Params &P, uint8_t *sm) {
     }
 }
 
-template <int NQ, bool CAUSAL>
+template <int NQ, bool CAUSAL, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap mlat, const __grid_constant__ CUtensorMap mrope, const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -818,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
         if (warp == kMmaWarp) mma_issuer<NQ>(P, sm);
-        else producer<NQ>(P, &mlat, &mrope, sm);
+        else producer<NQ, PAGED>(P, &mlat, &mrope, sm);
     }
     tc::fence_before();
     __syncthreads();
@@ -843,19 +854,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int NQ, bool CAUSAL>
+template <int NQ, bool CAUSAL, bool PAGED>
 cudaError_t launch_as(const CUtensorMap &ml, const CUtensorMap &mr, const Params &P, int grid, cudaStream_t st) {
     const size_t smem = smem_bytes<NQ>();
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NQ, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NQ, CAUSAL, PAGED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tc_kernel<NQ, CAUSAL><<<grid, kThreads, smem, st>>>(ml, mr, P);
+    attend_tc_kernel<NQ, CAUSAL, PAGED><<<grid, kThreads, smem, st>>>(ml, mr, P);
     return cudaGetLastError();
 }
 
 template <int NQ>
 cudaError_t launch(const CUtensorMap &ml, const CUtensorMap &mr, const Params &P, int grid, cudaStream_t st) {
-    return P.causal ? launch_as<NQ, true>(ml, mr, P, grid, st) : launch_as<NQ, false>(ml, mr, P, grid, st);
+    if (P.log2p > 0)
+        return P.causal ? launch_as<NQ, true, true>(ml, mr, P, grid, st) : launch_as<NQ, false, true>(ml, mr, P, grid, st);
+    return P.causal ? launch_as<NQ, true, false>(ml, mr, P, grid, st) : launch_as<NQ, false, false>(ml, mr, P, grid, st);
 }
 
 }  // namespace

@@ -256,6 +256,8 @@ __device__ __forceinline__ const uint8_t *kv_row(const uint8_t *kv, const int32_
 // Warp-cooperative: lane l holds request r_base + l of a 32-request window
 // and an inclusive prefix sum of the split counts.  Queries must come in
 // non-decreasing u order.  Every lane of the warp must call find() together.
+// PAGED: indptr counts blocks of 2^log2p rows (see request_len).
+template <bool PAGED = false>
 struct UnitCursor {
     const int32_t *indptr;
     const int32_t *last_page_len;   // block tables only
@@ -268,8 +270,8 @@ struct UnitCursor {
     __device__ void init(const int32_t *ip, int r_count, int64_t pages_len, int ns, int st, int lane,
                          int lp = 0, const int32_t *last = nullptr) {
         indptr = ip;
-        last_page_len = last;
-        log2p = lp;
+        last_page_len = PAGED ? last : nullptr;
+        log2p = PAGED ? lp : 0;
         R = r_count;
         num_pages = pages_len;
         num_splits = ns;
@@ -282,7 +284,8 @@ struct UnitCursor {
     __device__ void load(int lane) {
         const int r = r_base + lane;
         if (r < R) {
-            len = request_len(indptr, r, num_pages, &base, log2p, last_page_len);
+            len = PAGED ? request_len(indptr, r, num_pages, &base, log2p, last_page_len)
+                        : request_len(indptr, r, num_pages, &base);
             n = split_count(len, num_splits, split_tokens);
         } else {
             len = 0;
@@ -331,9 +334,9 @@ struct Tile {
 
 // Iterates this CTA's tiles in order: units u = blockIdx.x, +gridDim.x, ...
 // (each unit row group by row group), each unit cut into TILE-token tiles.
-template <int TILE>
+template <int TILE, bool PAGED = false>
 struct TileIter {
-    UnitCursor cur;
+    UnitCursor<PAGED> cur;
     long long u;
     int t, ntiles, start, count, r, k, n_r, base, grp;
     bool have_unit;
