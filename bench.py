@@ -86,9 +86,9 @@ def _spec(name):
     raise SystemExit("unknown workload %s (have %s)" % (name, [s.name for s in W.WORKLOADS]))
 
 
-def _plan_stats(inp, ns, st, page_size=1):
+def _plan_stats(inp, ns, st, page_size=1, plan_len=0):
     """Host-side split counts and the attend kernel's algorithmic bytes
-    (KV rows, page / block indices, indptr, q, partials)."""
+    (KV rows, page / block indices, indptr, q, partials, the work plan)."""
     lens = inp.lengths.cpu().numpy().astype(np.int64)
     n_r = np.maximum(1, np.minimum(ns, -(-lens // st)))
     used = int(n_r[lens > 0].sum())
@@ -96,7 +96,7 @@ def _plan_stats(inp, ns, st, page_size=1):
     total = int(lens.sum())
     R = len(lens)
     index_bytes = 4 * total if page_size == 1 else 4 * int((-(-lens // page_size)).sum()) + 4 * R
-    attend_bytes = (total * 576 + index_bytes + (R + 1) * 4 + R * rows_per_req * 576 * 2
+    attend_bytes = (total * 576 + index_bytes + (R + 1) * 4 + R * rows_per_req * 576 * 2 + 4 * plan_len
                     + used * rows_per_req * (512 * 2 + 4)
                     + int((ns - n_r).sum() + (lens == 0).sum()) * rows_per_req * 4)
     merge_bytes = used * rows_per_req * (512 * 2 + 4) + ns * R * rows_per_req * 4 + R * rows_per_req * (1024 + 4)
@@ -183,7 +183,11 @@ def run_gpu(args):
     R, qlen, H = spec.requests, spec.qlen, spec.heads
     S = R * qlen
     ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
-    stats = _plan_stats(inp, ns, st, args.page_size)
+    # Work plan: the units placed longest-first on the least loaded CTA, from
+    # the host-known lengths (host metadata, like the split rule above).
+    plan_h = None if args.no_plan else mla.plan_units(inp.lengths.cpu(), qlen, H, ns, st)
+    plan = None if plan_h is None else plan_h.to(dev)
+    stats = _plan_stats(inp, ns, st, args.page_size, 0 if plan_h is None else plan_h.numel())
     stream = torch.cuda.current_stream(dev)
 
     o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
@@ -197,7 +201,8 @@ def run_gpu(args):
         if ev:
             ev[0].record(strm)
         mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last, stream=strm)
+                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last, plan=plan,
+                   stream=strm)
         if ev:
             ev[1].record(strm)
         if args.three_call:
@@ -267,19 +272,23 @@ def run_gpu(args):
     lens_h = inp.lengths.cpu().pin_memory()
     last_h = last.cpu().pin_memory() if last is not None else None
     last_d = torch.empty_like(last) if last is not None else None
+    plan_hp = plan_h.pin_memory() if plan_h is not None else None
+    plan_d = torch.empty_like(plan) if plan is not None else None
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     q_d, gate_d = torch.empty_like(inp.q), torch.empty_like(inp.gate)
     pages_d, indptr_d, lens_d = torch.empty_like(inp.pages), torch.empty_like(inp.indptr), torch.empty_like(inp.lengths)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h, last_h) if t is not None)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h, last_h, plan_hp)
+              if t is not None)
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
         for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h),
-                     (last_d, last_h)):
+                     (last_d, last_h), (plan_d, plan_hp)):
             if d is not None:
                 d.copy_(h, non_blocking=True)
         mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, stream=stream)
+                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, plan=plan_d,
+                   stream=stream)
         if args.three_call:
             mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
             mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
@@ -329,6 +338,7 @@ def run_gpu(args):
             "workload": spec.name, "requests": R, "qlen": qlen, "heads": H, "rows": S,
             "kv_tokens": stats["kv_tokens"], "kv_bytes": stats["kv_tokens"] * 576,
             "num_splits": ns, "split_tokens": st, "work_units": stats["used_units"],
+            "work_plan": "round robin" if plan is None else "host LPT plan (longest unit first to the least loaded CTA)",
             "l2": "flushed before every timed step (256 MB write, outside the events)",
             "parallelism": "replicas" if ws > 1 else "single-gpu",
             "kv": "fp8-e4m3 paged (page size %d%s)" % (args.page_size, ", block tables" if args.page_size > 1 else ""),
@@ -489,6 +499,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--page-size", type=int, default=1,
                     help="KV cache as block tables of this many rows per block (power of two)")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="round-robin work units instead of the host LPT work plan")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     args = ap.parse_args()

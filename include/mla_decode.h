@@ -58,6 +58,7 @@ typedef int mla_status;
 #define MLA_DEV_BAD_PAGE 1u      /* a page index was outside [0, pool_rows)      */
 #define MLA_DEV_BAD_INDPTR 2u    /* indptr not monotone or beyond num_pages      */
 #define MLA_DEV_TIMEOUT 4u       /* a bounded device wait ran out                */
+#define MLA_DEV_BAD_PLAN 8u      /* a work plan did not fit this launch          */
 
 /*
  * mla_decode_attend -- split-KV attention of one decode step.
@@ -159,6 +160,53 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                    int num_requests, int qlen, int heads, float scale, float kv_scale,
                                    int num_splits, int split_tokens, void *o, float *lse,
                                    unsigned int flags, void *stream);
+
+/*
+ * mla_plan_units -- a work plan for the persistent attend kernel.
+ *
+ * The pages have no counterpart: the attend step's work units (request r,
+ * split k, query-row group g) are independent, and the kernel runs one
+ * CTA per SM that, by default, takes units u = b, b + G, b + 2G, ... in
+ * request-major order (u = (unit of (r, k)) * groups + g).  With contexts
+ * of mixed length that round robin leaves some CTAs with far more tiles
+ * than others.  This host routine, given the requests' token counts,
+ * assigns the units longest-first, each to the least loaded CTA (cost =
+ * its 128-token tiles plus a fixed start-up share), and writes
+ *   plan = [G, offsets[0 .. G], ids...]
+ * where CTA b takes ids[offsets[b] .. offsets[b + 1]) in increasing order.
+ * The split rule, shape and G must be those of the attend call that uses it.
+ *
+ *   host_lengths  int32 [num_requests], host: tokens per request (<= 0: empty).
+ *   sm_count      G; <= 0 takes the current device's SM count (the grid the
+ *                 attend kernel launches).
+ *   plan          int32 [plan_capacity], host, caller-owned; NULL asks for
+ *                 the size only.
+ * Returns the plan's length in int32 (2 + G + units), or a negative
+ * mla_status (MLA_ERR_INVALID: bad argument or plan_capacity too small).
+ */
+int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths,
+                       int num_splits, int split_tokens, int sm_count, int32_t *plan,
+                       int64_t plan_capacity);
+
+/*
+ * mla_decode_attend_planned -- mla_decode_attend_paged with a work plan.
+ *
+ * plan (int32 [plan_len], device, 4-byte aligned) as mla_plan_units wrote
+ * it, copied to the device; NULL is the round robin of
+ * mla_decode_attend_paged.  The outputs do not depend on the plan: each
+ * unit's partial is computed the same way on whichever CTA takes it.  A
+ * plan for another grid, offsets outside the buffer or ids not increasing
+ * within a CTA set MLA_DEV_BAD_PLAN and leave the affected units unwritten;
+ * an id past the last unit ends that CTA's list.  plan_len < 3 with a plan:
+ * MLA_ERR_INVALID; a plan with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
+ */
+mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv,
+                                     int64_t pool_rows, const int32_t *pages, int64_t num_pages,
+                                     const int32_t *indptr, const int32_t *last_page_len,
+                                     int page_size, int num_requests, int qlen, int heads,
+                                     float scale, float kv_scale, int num_splits,
+                                     int split_tokens, void *o, float *lse, unsigned int flags,
+                                     const int32_t *plan, int64_t plan_len, void *stream);
 
 /*
  * mla_merge_splits -- LSE merge of split partials into the latent.

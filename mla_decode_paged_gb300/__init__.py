@@ -27,9 +27,9 @@ from . import build as _build
 D_QK, D_LATENT, D_V = 576, 512, 128
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
 ATTEND_CAUSAL, ATTEND_Q_FP8 = 1, 2
-DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT = 1, 2, 4
+DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT, DEV_BAD_PLAN = 1, 2, 4, 8
 
-__all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "debug_gather",
+__all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "plan_units", "debug_gather",
            "kv_append", "device_status", "build", "library", "MlaError"]
 
 
@@ -67,6 +67,10 @@ def library() -> ctypes.CDLL:
                                          vp, vp, ctypes.c_uint, vp]
     lib.mla_decode_attend_paged.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
                                             i32, i32, vp, vp, ctypes.c_uint, vp]
+    lib.mla_decode_attend_planned.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
+                                              i32, i32, vp, vp, ctypes.c_uint, vp, i64, vp]
+    lib.mla_plan_units.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, i64]
+    lib.mla_plan_units.restype = i64
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.mla_merge_value_gate.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
@@ -74,7 +78,7 @@ def library() -> ctypes.CDLL:
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mla_kv_append.argtypes = [vp, i64, vp, i64, vp, i64, f32, vp, i64, vp]
-    for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
+    for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_decode_attend_planned", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
                  "mla_device_status", "mla_choose_splits", "mla_kv_append"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -120,7 +124,7 @@ def _as_u8(kv: torch.Tensor) -> torch.Tensor:
 
 
 def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
-           o=None, lse=None, causal=False, page_size=1, last_page_len=None, q_scale=1.0, stream=None):
+           o=None, lse=None, causal=False, page_size=1, last_page_len=None, q_scale=1.0, plan=None, stream=None):
     """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
     lse [num_splits, S, heads] f32)``.
 
@@ -134,6 +138,9 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     last block; ``mla_decode_attend_paged``).
     A ``q`` of dtype float8_e4m3fn / uint8 is an fp8 query (codes); its
     ``q_scale`` multiplies the softmax scale (``MLA_ATTEND_Q_FP8``).
+    ``plan``: a device int32 work plan from :func:`plan_units` for the same
+    lengths, split rule and shape (``mla_decode_attend_planned``); the
+    outputs are the same with or without it.
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
@@ -156,11 +163,15 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     if page_size > 1:
         _need(last_page_len is not None and last_page_len.dtype == torch.int32 and last_page_len.numel() == R
               and last_page_len.is_contiguous(), "page_size > 1 needs last_page_len int32 [R]")
-    st = library().mla_decode_attend_paged(
+    if plan is not None:
+        _need(plan.dtype == torch.int32 and plan.dim() == 1 and plan.is_contiguous() and plan.is_cuda,
+              "plan must be a contiguous int32 device tensor")
+    st = library().mla_decode_attend_planned(
         _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
         _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
         heads, float(scale) * float(q_scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o),
-        _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), ctypes.c_void_p(_stream(stream)))
+        _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), _ptr(plan),
+        0 if plan is None else plan.numel(), ctypes.c_void_p(_stream(stream)))
     _check(st, "mla_decode_attend")
     return o, lse
 
@@ -248,6 +259,25 @@ def choose_splits(num_requests, qlen, heads, max_len=0, total_len=0, sm_count=0,
     return int(ns), int(st.value)
 
 
+def plan_units(lengths, qlen, heads, num_splits, split_tokens, sm_count=0):
+    """Host work plan for :func:`attend` (``mla_plan_units``): the units
+    assigned longest-first to the least loaded of ``sm_count`` CTAs (0: the
+    current device's SMs).  Returns a CPU int32 tensor; copy it to the
+    device and pass it as ``attend(..., plan=)``."""
+    host = torch.as_tensor(lengths, dtype=torch.int32, device="cpu").contiguous()
+    lib = library()
+    args = (host.numel(), int(qlen), int(heads), ctypes.c_void_p(host.data_ptr()), int(num_splits),
+            int(split_tokens), int(sm_count))
+    n = lib.mla_plan_units(*args, None, 0)
+    if n < 0:
+        _check(int(n), "mla_plan_units")
+    plan = torch.empty(n, dtype=torch.int32)
+    n2 = lib.mla_plan_units(*args, ctypes.c_void_p(plan.data_ptr()), n)
+    if n2 < 0:
+        _check(int(n2), "mla_plan_units")
+    return plan
+
+
 def debug_gather(kv, pages, indptr, total_rows=None, stream=None):
     """Every request's KV rows in request order ([sum L, 576] uint8), gathered
     by the attend kernels' own row addressing."""
@@ -286,7 +316,7 @@ def kv_append(kv, kv_c, k_pe, slots, k_scale, *, stream=None):
 
 def device_status(stream=None) -> int:
     """Synchronise the stream, return and clear the device status bits
-    (DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT)."""
+    (DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT, DEV_BAD_PLAN)."""
     flags = ctypes.c_uint(0)
     _check(library().mla_device_status(ctypes.c_void_p(_stream(stream)), ctypes.byref(flags)),
            "mla_device_status")
@@ -294,17 +324,19 @@ def device_status(stream=None) -> int:
 
 
 def decode_step(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, *, heads=None, qlen=1,
-                num_splits=None, split_tokens=None, max_len=None, total_len=0, causal=False, stream=None):
+                num_splits=None, split_tokens=None, max_len=None, total_len=0, causal=False, plan=None,
+                stream=None):
     """The whole step (attend -> merge -> value_gate); returns
     ``(out, latent, lse)``.  Without a split plan one is chosen from
-    ``max_len`` (host-known longest request).  ``causal`` as in :func:`attend`."""
+    ``max_len`` (host-known longest request).  ``causal`` and ``plan`` as in
+    :func:`attend`."""
     heads = q.shape[1] if heads is None else heads
     if num_splits is None or split_tokens is None:
         if max_len is None:
             raise ValueError("give num_splits and split_tokens, or max_len for the split plan")
         num_splits, split_tokens = choose_splits(indptr.numel() - 1, qlen, heads, max_len, total_len)
     o, lse = attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, heads=heads,
-                    qlen=qlen, causal=causal, stream=stream)
+                    qlen=qlen, causal=causal, plan=plan, stream=stream)
     latent, lse_m = merge(o, lse, stream=stream)
     out = value_gate(latent, w_uv, gate, lengths, qlen, stream=stream)
     return out, latent, lse_m

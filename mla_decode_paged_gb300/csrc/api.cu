@@ -6,6 +6,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <string>
+#include <algorithm>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -22,7 +25,8 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
                              float *lse, bool causal, int log2p, const int32_t *last_page_len, bool q8,
-                             int grid, cudaStream_t st);
+                             const int32_t *plan, int64_t plan_len, int grid, cudaStream_t st);
+void attend_tc_shape(int rows, int *groups, int *nq);
 cudaError_t attend_tc_status(unsigned int *flags, bool clear);
 cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int rows, int heads,
                          void *latent, float *lse_out, cudaStream_t st);
@@ -101,7 +105,19 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                    const int32_t *last_page_len, int page_size, int num_requests, int qlen,
                                    int heads, float scale, float kv_scale, int num_splits, int split_tokens,
                                    void *o, float *lse, unsigned int flags, void *stream) {
+    return mla_decode_attend_planned(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, last_page_len,
+                                     page_size, num_requests, qlen, heads, scale, kv_scale, num_splits,
+                                     split_tokens, o, lse, flags, nullptr, 0, stream);
+}
+
+mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                     const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                                     const int32_t *last_page_len, int page_size, int num_requests, int qlen,
+                                     int heads, float scale, float kv_scale, int num_splits, int split_tokens,
+                                     void *o, float *lse, unsigned int flags, const int32_t *plan,
+                                     int64_t plan_len, void *stream) {
     if (flags & ~(MLA_ATTEND_CAUSAL | MLA_ATTEND_Q_FP8)) return fail(MLA_ERR_INVALID, "unknown flag bits");
+    if (plan && (plan_len < 3 || !aligned(plan, 4))) return fail(MLA_ERR_INVALID, "plan too short or misaligned");
     const bool q8 = (flags & MLA_ATTEND_Q_FP8) != 0;
     int log2p = 0;
     while ((1 << log2p) < page_size && log2p < 9) ++log2p;
@@ -133,6 +149,7 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
     if (causal && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "causal mask with the warp-MMA kernel");
     if (page_size > 1 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "page_size > 1 with the warp-MMA kernel");
     if (q8 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "fp8 query with the warp-MMA kernel");
+    if (plan && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "work plan with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_warp_mma()
                         ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
@@ -140,8 +157,8 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                                  split_tokens, o, lse, device_sms(), st)
                         : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                split_tokens, o, lse, causal, log2p, last_page_len, q8, device_sms(),
-                                                st);
+                                                split_tokens, o, lse, causal, log2p, last_page_len, q8, plan,
+                                                plan_len, device_sms(), st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }
@@ -270,6 +287,60 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
     }
     if (split_tokens) *split_tokens = best_st;
     return best_ns;
+}
+
+int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
+                       int split_tokens, int sm_count, int32_t *plan, int64_t plan_capacity) {
+    if (num_requests < 0 || qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS ||
+        num_splits < 1 || num_splits > MLA_MAX_SPLITS || split_tokens < 1 || (num_requests > 0 && !host_lengths))
+        return fail(MLA_ERR_INVALID, "bad plan arguments");
+    if (sm_count <= 0) sm_count = device_sms();
+    int groups, nq;
+    mla::attend_tc_shape(qlen * heads, &groups, &nq);
+    // Units in the kernels' numbering (request-major, then split, then row
+    // group), each with a cost in tiles plus a fixed per-unit share.
+    struct Unit {
+        double cost;
+        int id;
+    };
+    std::vector<Unit> units;
+    int id = 0;
+    for (int r = 0; r < num_requests; ++r) {
+        const int L = host_lengths[r] > 0 ? host_lengths[r] : 0;
+        int n = (L + split_tokens - 1) / split_tokens;
+        n = n < 1 ? 1 : (n > num_splits ? num_splits : n);
+        const int b = L / n, m = L % n;
+        for (int k = 0; k < n; ++k) {
+            const int count = b + (k < m ? 1 : 0);
+            const double cost = (count + 127) / 128 + (count > 0 ? 0.5 : 0.2);
+            for (int g = 0; g < groups; ++g) units.push_back({cost, id++});
+        }
+    }
+    const int64_t need = 2 + (int64_t)sm_count + (int64_t)units.size();
+    if (!plan) return need;
+    if (plan_capacity < need) return fail(MLA_ERR_INVALID, "plan buffer too small");
+    // Longest first, each to the least loaded CTA (ties: lowest index).
+    std::vector<Unit> order = units;
+    std::stable_sort(order.begin(), order.end(), [](const Unit &x, const Unit &y) { return x.cost > y.cost; });
+    std::vector<double> load(sm_count, 0.0);
+    std::vector<std::vector<int>> mine(sm_count);
+    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<std::pair<double, int>>> heap;
+    for (int c = 0; c < sm_count; ++c) heap.push({0.0, c});
+    for (const Unit &u : order) {
+        auto top = heap.top();
+        heap.pop();
+        mine[top.second].push_back(u.id);
+        heap.push({top.first + u.cost, top.second});
+    }
+    plan[0] = sm_count;
+    int64_t pos = 0;
+    for (int c = 0; c < sm_count; ++c) {
+        std::sort(mine[c].begin(), mine[c].end());   // a CTA walks its units in increasing order
+        plan[1 + c] = (int32_t)pos;
+        for (int x : mine[c]) plan[2 + sm_count + pos++] = x;
+    }
+    plan[1 + sm_count] = (int32_t)pos;
+    return need;
 }
 
 mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *k_pe, int64_t k_pe_row_stride,

@@ -116,6 +116,8 @@ struct Params {
     int R, qlen, heads, num_splits, split_tokens, row_groups, nq, causal;
     int log2p;                          // blocks of 2^log2p rows (0: flat token rows)
     int q8;                             // q holds e4m3 codes (row stride in bytes)
+    const int32_t *plan;                // work plan (null: units dealt round robin)
+    int64_t plan_len;                   // its length in int32
     const int32_t *last_page_len;       // rows used in each request's last block (log2p > 0)
     float sc_log2;
     float kv_scale;
@@ -229,9 +231,10 @@ __device__ void producer(const Params &P, const CUtensorMap *mlat, const CUtenso
     TileIter<C::T, PAGED> iter;
     if (PAGED)
         iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, P.log2p,
-                  P.last_page_len);
+                  P.last_page_len, P.plan, P.plan_len);
     else
-        iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane);
+        iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, 0, nullptr,
+                  P.plan, P.plan_len);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -888,7 +891,7 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
                              const int32_t *pages, int64_t num_pages, const int32_t *indptr, int R, int qlen,
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
                              float *lse, bool causal, int log2p, const int32_t *last_page_len, bool q8,
-                             int grid, cudaStream_t st) {
+                             const int32_t *plan, int64_t plan_len, int grid, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap ml, mr;
@@ -918,6 +921,8 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
     P.causal = causal ? 1 : 0;
     P.log2p = log2p;
     P.q8 = q8 ? 1 : 0;
+    P.plan = plan;
+    P.plan_len = plan_len;
     P.last_page_len = last_page_len;
     P.sc_log2 = scale * kv_scale * 1.4426950408889634f;
     P.kv_scale = kv_scale;

@@ -332,29 +332,68 @@ struct Tile {
     bool valid;
 };
 
-// Iterates this CTA's tiles in order: units u = blockIdx.x, +gridDim.x, ...
-// (each unit row group by row group), each unit cut into TILE-token tiles.
+// Iterates this CTA's tiles in order, each unit (request, split, row group;
+// numbered request-major, u = unit * groups + group) cut into TILE-token
+// tiles.  Units u = blockIdx.x, +gridDim.x, ... by default; with a work
+// plan (int32: [G, offsets[G + 1], unit ids]; this CTA's ids ascending) the
+// CTA takes ids[offsets[b] .. offsets[b + 1]).
 template <int TILE, bool PAGED = false>
 struct TileIter {
     UnitCursor<PAGED> cur;
     long long u;
     int t, ntiles, start, count, r, k, n_r, base, grp;
     bool have_unit;
+    const int32_t *plan_ids;   // null: round robin
+    int plan_pos, plan_end;
 
     int row_groups;
     __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
-                         int groups, int lane, int log2p = 0, const int32_t *last_page_len = nullptr) {
+                         int groups, int lane, int log2p = 0, const int32_t *last_page_len = nullptr,
+                         const int32_t *plan = nullptr, int64_t plan_len = 0) {
         cur.init(indptr, R, num_pages, num_splits, split_tokens, lane, log2p, last_page_len);
         row_groups = groups;
         u = (long long)blockIdx.x - gridDim.x;
         have_unit = false;
+        plan_ids = nullptr;
+        if (plan) {
+            // A plan for another grid, or offsets outside the buffer: flagged, no work.
+            plan_ids = plan + 2 + gridDim.x;
+            plan_pos = plan_end = 0;
+            u = -1;   // ids must increase from here
+            const int64_t ids = plan_len - 2 - (int64_t)gridDim.x;
+            if (plan_len < 2 + (int64_t)gridDim.x || __ldg(plan) != (int)gridDim.x) {
+                flag(MLA_DEV_BAD_PLAN);
+            } else {
+                const int a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
+                if (a < 0 || b < a || (int64_t)b > ids) flag(MLA_DEV_BAD_PLAN);
+                else {
+                    plan_pos = a;
+                    plan_end = b;
+                }
+            }
+        }
     }
 
     __device__ Tile next(int lane) {
         Tile T;
         T.valid = false;
         if (!have_unit || t >= ntiles) {
-            u += gridDim.x;
+            if (plan_ids) {
+                if (plan_pos >= plan_end) {
+                    have_unit = false;
+                    return T;
+                }
+                const int nu = __ldg(plan_ids + plan_pos++);
+                if (nu <= u) {   // the cursor only walks forward
+                    flag(MLA_DEV_BAD_PLAN);
+                    plan_pos = plan_end;
+                    have_unit = false;
+                    return T;
+                }
+                u = nu;
+            } else {
+                u += gridDim.x;
+            }
             int len;
             if (!cur.find(u / row_groups, lane, &r, &k, &n_r, &len, &base)) {
                 have_unit = false;
