@@ -248,14 +248,19 @@ def split_plan(L: int, num_splits: int, split_tokens: int):
 
 def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
                   num_splits, split_tokens, requests=None, causal=False, page_size=1, last_page_len=None,
-                  q_fp8=False):
+                  q_fp8=False, ranges=None):
     """Per-split partials: o [num_splits, S, H, 512] (float64) and lse
     [num_splits, S, H]; each used split is the attention restricted to its
     token range (``m1c_inputs``: new partials o [splits, S, 12, 512], LSE
     [splits, S, 12], merged afterwards).  Unused splits hold lse = -inf and
     o = NaN (their o is unspecified).  With ``causal``, a split's partial for
     a row covers the tokens of the split's range that the row sees; a row
-    that sees none of them gets lse = -inf there."""
+    that sees none of them gets lse = -inf there.
+
+    The pages fix the partials but not where a request is cut: by default
+    the ranges are :func:`split_plan`'s; ``ranges`` (a mapping or sequence
+    r -> [(start, end), ...], split k covering tokens start..end-1) gives
+    them explicitly (``split_tokens`` is then unused)."""
     q = np.asarray(q_bits)
     R = len(indptr) - 1
     S = R * qlen
@@ -268,7 +273,8 @@ def attend_splits(q_bits, kv_codes, pages, indptr, scale, kv_scale, heads, qlen,
         K = dequant(gather_rows(kv_codes, pages, indptr, r, page_size, last_page_len), kv_scale)
         rows = query_rows(q, r * qlen, (r + 1) * qlen, heads, q_fp8)
         vis = causal_visible(K.shape[0], qlen, heads) if causal else np.full(qlen * heads, K.shape[0])
-        for k, (a, b) in enumerate(split_plan(K.shape[0], num_splits, split_tokens)):
+        cuts = split_plan(K.shape[0], num_splits, split_tokens) if ranges is None else ranges[r]
+        for k, (a, b) in enumerate(cuts):
             lat, l, _ = attend_rows(rows, K[a:b], scale, vis - a)
             if b > a:
                 o[k, r * qlen:(r + 1) * qlen] = lat.reshape(qlen, heads, D_LATENT)

@@ -219,6 +219,52 @@ def test_merge_of_random_partition_equals_unsplit():
         assert np.allclose(ms[0], lse[r], atol=1e-12)
 
 
+def _random_ranges(lengths, num_splits, rng):
+    """A random partition of each request's tokens into 1..num_splits
+    consecutive ranges (some possibly empty)."""
+    out = []
+    for L in lengths:
+        n = int(rng.integers(1, num_splits + 1))
+        cuts = np.sort(rng.integers(0, L + 1, size=n - 1)) if L > 0 else np.zeros(n - 1, dtype=int)
+        edges = [0, *cuts.tolist(), int(L)]
+        out.append(list(zip(edges, edges[1:])))
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_merge_over_explicit_ranges_equals_unsplit(seed):
+    """Any partition of the tokens, merged by LSE, gives the unsplit
+    attention: the identity every split layout rests on."""
+    inp = W.make_inputs(1, lengths=[0, 1, 17, 128, 129, 300])
+    a = oracle_args(inp)
+    lat, lse = O.attend(**a)
+    rng = np.random.default_rng(seed)
+    rg = _random_ranges(i32(inp.lengths), 5, rng)
+    o, ls = O.attend_splits(**a, num_splits=5, split_tokens=1, ranges=rg)
+    for r, cuts in enumerate(rg):           # splits past a request's ranges stay unused
+        assert np.all(np.isneginf(ls[len(cuts):, r]))
+        for k, (x, y) in enumerate(cuts):
+            assert (x == y) == bool(np.all(np.isneginf(ls[k, r])))
+    mlat, mlse = O.merge(o, ls)
+    assert np.allclose(mlat, lat, atol=1e-12, rtol=1e-12)
+    assert np.array_equal(np.isneginf(mlse), np.isneginf(lse))
+    f = np.isfinite(lse)
+    assert np.allclose(mlse[f], lse[f], atol=1e-12)
+
+
+def test_explicit_ranges_causal_merge_equals_unsplit():
+    a, _, _, _ = _spec_like(seed=3)
+    lens = [int(a["indptr"][r + 1] - a["indptr"][r]) for r in range(len(a["indptr"]) - 1)]
+    rg = _random_ranges(lens, 4, np.random.default_rng(9))
+    lat, lse = O.attend(**a, causal=True)
+    o, ls = O.attend_splits(**a, num_splits=4, split_tokens=1, causal=True, ranges=rg)
+    mlat, mlse = O.merge(o, ls)
+    assert np.allclose(mlat, lat, atol=1e-12, rtol=1e-12)
+    assert np.array_equal(np.isneginf(mlse), np.isneginf(lse))
+    f = np.isfinite(lse)
+    assert np.allclose(mlse[f], lse[f], atol=1e-12)
+
+
 def test_merge_matches_brute_and_skips_empty():
     o_t, lse_t = W.make_partials(5, 4, 3, seed=1)
     o = O.bf16_to_f64(bf16_bits(o_t))[..., :8]
