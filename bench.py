@@ -86,11 +86,25 @@ def _spec(name):
     raise SystemExit("unknown workload %s (have %s)" % (name, [s.name for s in W.WORKLOADS]))
 
 
-def _plan_stats(inp, ns, st, page_size=1, plan_len=0):
+def _plan_splits(plan, R):
+    """Splits per request (n_r) of a work plan (items {r, k | n_r << 9 | ...}))."""
+    p = plan.numpy().astype(np.int64)
+    G = int(p[0])
+    it = p[G + 2:].reshape(-1, 4)
+    n_r = np.ones(R, dtype=np.int64)
+    n_r[it[:, 0]] = (it[:, 1] >> 9) & 511
+    return n_r
+
+
+def _plan_stats(inp, ns, st, page_size=1, plan=None):
     """Host-side split counts and the attend kernel's algorithmic bytes
     (KV rows, page / block indices, indptr, q, partials, the work plan)."""
     lens = inp.lengths.cpu().numpy().astype(np.int64)
-    n_r = np.maximum(1, np.minimum(ns, -(-lens // st)))
+    if plan is None:
+        n_r = np.maximum(1, np.minimum(ns, -(-lens // st)))
+    else:
+        n_r = _plan_splits(plan, len(lens))
+    plan_len = 0 if plan is None else plan.numel()
     used = int(n_r[lens > 0].sum())
     rows_per_req = inp.qlen * inp.heads
     total = int(lens.sum())
@@ -183,11 +197,15 @@ def run_gpu(args):
     R, qlen, H = spec.requests, spec.qlen, spec.heads
     S = R * qlen
     ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
-    # Work plan: the units placed longest-first on the least loaded CTA, from
-    # the host-known lengths (host metadata, like the split rule above).
-    plan_h = None if args.no_plan else mla.plan_units(inp.lengths.cpu(), qlen, H, ns, st)
+    # Work plan from the host-known lengths (host metadata, like the split
+    # rule above): the requests cut so that every CTA gets about the same
+    # number of tiles, at most ns splits each; the partials then need only
+    # the splits the plan used.
+    plan_h = None
+    if not args.no_plan:
+        plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
     plan = None if plan_h is None else plan_h.to(dev)
-    stats = _plan_stats(inp, ns, st, args.page_size, 0 if plan_h is None else plan_h.numel())
+    stats = _plan_stats(inp, ns, st, args.page_size, plan_h)
     stream = torch.cuda.current_stream(dev)
 
     o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
@@ -337,8 +355,8 @@ def run_gpu(args):
         "config": {
             "workload": spec.name, "requests": R, "qlen": qlen, "heads": H, "rows": S,
             "kv_tokens": stats["kv_tokens"], "kv_bytes": stats["kv_tokens"] * 576,
-            "num_splits": ns, "split_tokens": st, "work_units": stats["used_units"],
-            "work_plan": "round robin" if plan is None else "host LPT plan (longest unit first to the least loaded CTA)",
+            "num_splits": ns, "split_tokens": st if plan is None else None, "work_units": stats["used_units"],
+            "work_plan": "round robin" if plan is None else "host balanced plan (requests cut at tile boundaries so every CTA gets about the same tiles)",
             "l2": "flushed before every timed step (256 MB write, outside the events)",
             "parallelism": "replicas" if ws > 1 else "single-gpu",
             "kv": "fp8-e4m3 paged (page size %d%s)" % (args.page_size, ", block tables" if args.page_size > 1 else ""),
@@ -500,7 +518,7 @@ def main():
     ap.add_argument("--page-size", type=int, default=1,
                     help="KV cache as block tables of this many rows per block (power of two)")
     ap.add_argument("--no-plan", action="store_true",
-                    help="round-robin work units instead of the host LPT work plan")
+                    help="round-robin work units under the split rule instead of the host work plan")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     args = ap.parse_args()

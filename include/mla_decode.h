@@ -162,43 +162,61 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                    unsigned int flags, void *stream);
 
 /*
- * mla_plan_units -- a work plan for the persistent attend kernel.
+ * mla_plan_units -- a balanced work plan for the persistent attend kernel.
  *
- * The pages have no counterpart: the attend step's work units (request r,
- * split k, query-row group g) are independent, and the kernel runs one
- * CTA per SM that, by default, takes units u = b, b + G, b + 2G, ... in
- * request-major order (u = (unit of (r, k)) * groups + g).  With contexts
- * of mixed length that round robin leaves some CTAs with far more tiles
- * than others.  This host routine, given the requests' token counts,
- * assigns the units longest-first, each to the least loaded CTA (cost =
- * its 128-token tiles plus a fixed start-up share), and writes
- *   plan = [G, offsets[0 .. G], ids...]
- * where CTA b takes ids[offsets[b] .. offsets[b + 1]) in increasing order.
- * The split rule, shape and G must be those of the attend call that uses it.
+ * The pages have no counterpart: they fix the partials (one per split of a
+ * request, merged by LSE afterwards) but not where a request is cut.  The
+ * attend kernel runs one CTA per SM; by default each takes whole units
+ * (request, split, query-row group) round robin under the split rule of
+ * mla_decode_attend, which leaves some CTAs with far more 128-token tiles
+ * than others when contexts differ in length.  This host routine, given the
+ * requests' token counts, cuts the requests into splits itself: it fills
+ * the CTAs in request order, each up to one budget of tiles (plus a fixed
+ * share per split), cutting a request at a tile boundary where a CTA fills
+ * up, with the smallest budget that fits the grid and at most num_splits
+ * splits per request.  With g query-row groups (rows = qlen * heads cut
+ * into groups of at most 48) it fills G / g virtual CTAs and gives virtual
+ * CTA v's list to CTAs v * g + j, row group j.
+ *
+ * Layout (int32): plan = [G, offsets[0 .. G], items...], CTA b takes items
+ * offsets[b] .. offsets[b + 1] - 1, each MLA_PLAN_ITEM_WORDS int32
+ *   { r, k | n_r << 9 | group << 18, start, count }:
+ * split k (0-based) of the n_r splits of request r covers its tokens
+ * [start, start + count) for query-row group `group`; the splits of a
+ * request are consecutive ranges that cover all its tokens (an empty
+ * request has one split of count 0).
  *
  *   host_lengths  int32 [num_requests], host: tokens per request (<= 0: empty).
+ *   num_splits    most splits of one request (the partial buffers' split
+ *                 dimension of the attend call that uses the plan).
  *   sm_count      G; <= 0 takes the current device's SM count (the grid the
  *                 attend kernel launches).
  *   plan          int32 [plan_capacity], host, caller-owned; NULL asks for
  *                 the size only.
- * Returns the plan's length in int32 (2 + G + units), or a negative
- * mla_status (MLA_ERR_INVALID: bad argument or plan_capacity too small).
+ *   splits_used   optional out: the most splits any request got (<= num_splits).
+ * Returns the plan's length in int32, or a negative mla_status
+ * (MLA_ERR_INVALID: bad argument or plan_capacity too small;
+ * MLA_ERR_UNSUPPORTED: fewer SMs than query-row groups).
  */
+#define MLA_PLAN_ITEM_WORDS 4
 int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths,
-                       int num_splits, int split_tokens, int sm_count, int32_t *plan,
-                       int64_t plan_capacity);
+                       int num_splits, int sm_count, int32_t *plan, int64_t plan_capacity,
+                       int *splits_used);
 
 /*
  * mla_decode_attend_planned -- mla_decode_attend_paged with a work plan.
  *
  * plan (int32 [plan_len], device, 4-byte aligned) as mla_plan_units wrote
  * it, copied to the device; NULL is the round robin of
- * mla_decode_attend_paged.  The outputs do not depend on the plan: each
- * unit's partial is computed the same way on whichever CTA takes it.  A
- * plan for another grid, offsets outside the buffer or ids not increasing
- * within a CTA set MLA_DEV_BAD_PLAN and leave the affected units unwritten;
- * an id past the last unit ends that CTA's list.  plan_len < 3 with a plan:
- * MLA_ERR_INVALID; a plan with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
+ * mla_decode_attend_paged.  The plan's splits replace the split rule
+ * (split_tokens is then unused): each split's partial o / lse is the
+ * attention over its token range, unused splits k >= n_r get lse = -inf,
+ * and the merged result is the same attention up to rounding.  A plan for
+ * another grid, offsets outside the buffer, or an item outside the launch
+ * (r >= num_requests, k >= n_r, n_r > num_splits, group >= the row groups,
+ * a range past the request's tokens) sets MLA_DEV_BAD_PLAN and ends that
+ * CTA's list, leaving its remaining splits unwritten.  plan_len < 3 with a
+ * plan: MLA_ERR_INVALID; a plan with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv,
                                      int64_t pool_rows, const int32_t *pages, int64_t num_pages,

@@ -69,7 +69,7 @@ def library() -> ctypes.CDLL:
                                             i32, i32, vp, vp, ctypes.c_uint, vp]
     lib.mla_decode_attend_planned.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
                                               i32, i32, vp, vp, ctypes.c_uint, vp, i64, vp]
-    lib.mla_plan_units.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, i64]
+    lib.mla_plan_units.argtypes = [i32, i32, i32, vp, i32, i32, vp, i64, ctypes.POINTER(ctypes.c_int)]
     lib.mla_plan_units.restype = i64
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
@@ -139,8 +139,8 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     A ``q`` of dtype float8_e4m3fn / uint8 is an fp8 query (codes); its
     ``q_scale`` multiplies the softmax scale (``MLA_ATTEND_Q_FP8``).
     ``plan``: a device int32 work plan from :func:`plan_units` for the same
-    lengths, split rule and shape (``mla_decode_attend_planned``); the
-    outputs are the same with or without it.
+    lengths and shape (``mla_decode_attend_planned``): its splits replace
+    the ``split_tokens`` rule; the merged result is the same up to rounding.
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
@@ -259,23 +259,26 @@ def choose_splits(num_requests, qlen, heads, max_len=0, total_len=0, sm_count=0,
     return int(ns), int(st.value)
 
 
-def plan_units(lengths, qlen, heads, num_splits, split_tokens, sm_count=0):
-    """Host work plan for :func:`attend` (``mla_plan_units``): the units
-    assigned longest-first to the least loaded of ``sm_count`` CTAs (0: the
-    current device's SMs).  Returns a CPU int32 tensor; copy it to the
-    device and pass it as ``attend(..., plan=)``."""
+def plan_units(lengths, qlen, heads, num_splits, sm_count=0):
+    """Balanced host work plan for :func:`attend` (``mla_plan_units``): the
+    requests cut into at most ``num_splits`` splits so that each of
+    ``sm_count`` CTAs (0: the current device's SMs) gets about the same
+    number of tiles.  Returns ``(plan, splits_used)``: a CPU int32 tensor
+    (copy it to the device and pass it as ``attend(..., plan=)``) and the
+    most splits any request got (the smallest ``num_splits`` the partial
+    buffers need)."""
     host = torch.as_tensor(lengths, dtype=torch.int32, device="cpu").contiguous()
     lib = library()
-    args = (host.numel(), int(qlen), int(heads), ctypes.c_void_p(host.data_ptr()), int(num_splits),
-            int(split_tokens), int(sm_count))
-    n = lib.mla_plan_units(*args, None, 0)
+    used = ctypes.c_int(0)
+    args = (host.numel(), int(qlen), int(heads), ctypes.c_void_p(host.data_ptr()), int(num_splits), int(sm_count))
+    n = lib.mla_plan_units(*args, None, 0, ctypes.byref(used))
     if n < 0:
         _check(int(n), "mla_plan_units")
     plan = torch.empty(n, dtype=torch.int32)
-    n2 = lib.mla_plan_units(*args, ctypes.c_void_p(plan.data_ptr()), n)
+    n2 = lib.mla_plan_units(*args, ctypes.c_void_p(plan.data_ptr()), n, ctypes.byref(used))
     if n2 < 0:
         _check(int(n2), "mla_plan_units")
-    return plan
+    return plan, int(used.value)
 
 
 def debug_gather(kv, pages, indptr, total_rows=None, stream=None):

@@ -7,7 +7,6 @@
 #include <cstdlib>
 #include <string>
 #include <algorithm>
-#include <queue>
 #include <utility>
 #include <vector>
 
@@ -289,55 +288,121 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
     return best_ns;
 }
 
+namespace {
+
+// Cost model of the work plan, in tenths of a 128-token tile: a tile, the
+// fixed share of a split (query prep, epilogue) and an empty request.
+constexpr int64_t kPlanTile = 10, kPlanPiece = 5, kPlanEmpty = 2;
+
+struct PlanPiece {
+    int r, k, start, count;
+};
+
+// Greedy contiguous fill of the requests' tiles, in request order, into
+// virtual CTAs of at most `budget` each; a request is cut at tile
+// boundaries where a CTA fills up.  Returns the CTAs used (V + 1 when more
+// than V would be needed or a request would need more than max_splits
+// pieces); pieces are appended per CTA when `out` is given.
+int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_splits,
+              std::vector<std::vector<PlanPiece>> *out) {
+    int v = 0;
+    int64_t load = 0;
+    if (out) out->assign(V, {});
+    for (int r = 0; r < R; ++r) {
+        const int L = lengths[r] > 0 ? lengths[r] : 0;
+        if (L == 0) {
+            if (load > 0 && load + kPlanEmpty > budget) {
+                if (++v >= V) return V + 1;
+                load = 0;
+            }
+            load += kPlanEmpty;
+            if (out) (*out)[v].push_back({r, 0, 0, 0});
+            continue;
+        }
+        const int ntiles = (L + 127) / 128;
+        int done = 0, k = 0;
+        while (done < ntiles) {
+            const int64_t room = budget - load;
+            if (load > 0 && room < kPlanPiece + kPlanTile) {
+                if (++v >= V) return V + 1;
+                load = 0;
+                continue;
+            }
+            int64_t take = (room - kPlanPiece) / kPlanTile;
+            if (take < 1) take = 1;
+            if (take > ntiles - done) take = ntiles - done;
+            if (++k > max_splits) return V + 1;
+            if (out) {
+                const int start = done * 128;
+                const int count = (int)std::min<int64_t>((int64_t)take * 128, (int64_t)L - start);
+                (*out)[v].push_back({r, k - 1, start, count});
+            }
+            load += take * kPlanTile + kPlanPiece;
+            done += (int)take;
+        }
+    }
+    return v + 1;
+}
+
+}  // namespace
+
 int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
-                       int split_tokens, int sm_count, int32_t *plan, int64_t plan_capacity) {
+                       int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
     if (num_requests < 0 || qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS ||
-        num_splits < 1 || num_splits > MLA_MAX_SPLITS || split_tokens < 1 || (num_requests > 0 && !host_lengths))
+        num_splits < 1 || num_splits > MLA_MAX_SPLITS || (num_requests > 0 && !host_lengths))
         return fail(MLA_ERR_INVALID, "bad plan arguments");
     if (sm_count <= 0) sm_count = device_sms();
     int groups, nq;
     mla::attend_tc_shape(qlen * heads, &groups, &nq);
-    // Units in the kernels' numbering (request-major, then split, then row
-    // group), each with a cost in tiles plus a fixed per-unit share.
-    struct Unit {
-        double cost;
-        int id;
-    };
-    std::vector<Unit> units;
-    int id = 0;
-    for (int r = 0; r < num_requests; ++r) {
-        const int L = host_lengths[r] > 0 ? host_lengths[r] : 0;
-        int n = (L + split_tokens - 1) / split_tokens;
-        n = n < 1 ? 1 : (n > num_splits ? num_splits : n);
-        const int b = L / n, m = L % n;
-        for (int k = 0; k < n; ++k) {
-            const int count = b + (k < m ? 1 : 0);
-            const double cost = (count + 127) / 128 + (count > 0 ? 0.5 : 0.2);
-            for (int g = 0; g < groups; ++g) units.push_back({cost, id++});
-        }
+    // Each row group of a request runs on its own CTA; the plan fills
+    // V = G / groups virtual CTAs and gives virtual CTA v's items to CTAs
+    // v * groups + g (row group g), so a request's groups read the same KV
+    // tiles at about the same time.
+    const int V = sm_count / groups;
+    if (V < 1) return fail(MLA_ERR_UNSUPPORTED, "fewer SMs than query-row groups");
+    // Smallest budget whose fill fits V CTAs within num_splits pieces per
+    // request (the fill with an unbounded budget always fits: one CTA, one
+    // piece per request).
+    int64_t total = 0;
+    for (int r = 0; r < num_requests; ++r)
+        total += host_lengths[r] > 0 ? ((host_lengths[r] + 127) / 128) * kPlanTile + kPlanPiece : kPlanEmpty;
+    int64_t lo = 0, hi = total + kPlanPiece + kPlanTile;
+    while (hi - lo > 1) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (plan_fill(host_lengths, num_requests, mid, V, num_splits, nullptr) <= V) hi = mid;
+        else lo = mid;
     }
-    const int64_t need = 2 + (int64_t)sm_count + (int64_t)units.size();
+    std::vector<std::vector<PlanPiece>> vc;
+    plan_fill(host_lengths, num_requests, hi, V, num_splits, &vc);
+    // pieces per request (n_r) and the plan's size
+    std::vector<int> n_r(num_requests > 0 ? num_requests : 1, 1);
+    int64_t items = 0;
+    int used = 1;
+    for (const auto &list : vc)
+        for (const PlanPiece &pc : list) {
+            n_r[pc.r] = std::max(n_r[pc.r], pc.k + 1);
+            used = std::max(used, pc.k + 1);
+            items += groups;
+        }
+    if (splits_used) *splits_used = used;
+    const int64_t need = 2 + (int64_t)sm_count + (int64_t)MLA_PLAN_ITEM_WORDS * items;
     if (!plan) return need;
     if (plan_capacity < need) return fail(MLA_ERR_INVALID, "plan buffer too small");
-    // Longest first, each to the least loaded CTA (ties: lowest index).
-    std::vector<Unit> order = units;
-    std::stable_sort(order.begin(), order.end(), [](const Unit &x, const Unit &y) { return x.cost > y.cost; });
-    std::vector<double> load(sm_count, 0.0);
-    std::vector<std::vector<int>> mine(sm_count);
-    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<std::pair<double, int>>> heap;
-    for (int c = 0; c < sm_count; ++c) heap.push({0.0, c});
-    for (const Unit &u : order) {
-        auto top = heap.top();
-        heap.pop();
-        mine[top.second].push_back(u.id);
-        heap.push({top.first + u.cost, top.second});
-    }
     plan[0] = sm_count;
+    int32_t *it = plan + 2 + sm_count;
     int64_t pos = 0;
-    for (int c = 0; c < sm_count; ++c) {
-        std::sort(mine[c].begin(), mine[c].end());   // a CTA walks its units in increasing order
-        plan[1 + c] = (int32_t)pos;
-        for (int x : mine[c]) plan[2 + sm_count + pos++] = x;
+    for (int b = 0; b < sm_count; ++b) {
+        plan[1 + b] = (int32_t)pos;
+        const int v = b / groups, g = b % groups;
+        if (v >= V) continue;
+        for (const PlanPiece &pc : vc[v]) {
+            it[0] = pc.r;
+            it[1] = pc.k | (n_r[pc.r] << 9) | (g << 18);
+            it[2] = pc.start;
+            it[3] = pc.count;
+            it += MLA_PLAN_ITEM_WORDS;
+            ++pos;
+        }
     }
     plan[1 + sm_count] = (int32_t)pos;
     return need;

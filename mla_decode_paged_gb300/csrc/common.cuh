@@ -334,16 +334,22 @@ struct Tile {
 
 // Iterates this CTA's tiles in order, each unit (request, split, row group;
 // numbered request-major, u = unit * groups + group) cut into TILE-token
-// tiles.  Units u = blockIdx.x, +gridDim.x, ... by default; with a work
-// plan (int32: [G, offsets[G + 1], unit ids]; this CTA's ids ascending) the
-// CTA takes ids[offsets[b] .. offsets[b + 1]).
+// tiles.  Units u = blockIdx.x, +gridDim.x, ... by default.  With a work
+// plan (int32: [G, offsets[G + 1], items]) the CTA takes the items
+// offsets[b] .. offsets[b + 1] - 1, each four int32
+//   {r, k | n_r << 9 | group << 18, start, count}:
+// split k of n_r of request r covers its tokens [start, start + count).  An
+// item that does not fit the launch flags MLA_DEV_BAD_PLAN and ends the
+// CTA's list.
+constexpr int kPlanItemWords = MLA_PLAN_ITEM_WORDS;
+
 template <int TILE, bool PAGED = false>
 struct TileIter {
     UnitCursor<PAGED> cur;
     long long u;
     int t, ntiles, start, count, r, k, n_r, base, grp;
     bool have_unit;
-    const int32_t *plan_ids;   // null: round robin
+    const int32_t *plan_items;   // null: round robin
     int plan_pos, plan_end;
 
     int row_groups;
@@ -354,18 +360,17 @@ struct TileIter {
         row_groups = groups;
         u = (long long)blockIdx.x - gridDim.x;
         have_unit = false;
-        plan_ids = nullptr;
+        plan_items = nullptr;
         if (plan) {
             // A plan for another grid, or offsets outside the buffer: flagged, no work.
-            plan_ids = plan + 2 + gridDim.x;
+            plan_items = plan + 2 + gridDim.x;
             plan_pos = plan_end = 0;
-            u = -1;   // ids must increase from here
-            const int64_t ids = plan_len - 2 - (int64_t)gridDim.x;
+            const int64_t items = (plan_len - 2 - (int64_t)gridDim.x) / kPlanItemWords;
             if (plan_len < 2 + (int64_t)gridDim.x || __ldg(plan) != (int)gridDim.x) {
                 flag(MLA_DEV_BAD_PLAN);
             } else {
                 const int a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
-                if (a < 0 || b < a || (int64_t)b > ids) flag(MLA_DEV_BAD_PLAN);
+                if (a < 0 || b < a || (int64_t)b > items) flag(MLA_DEV_BAD_PLAN);
                 else {
                     plan_pos = a;
                     plan_end = b;
@@ -374,33 +379,48 @@ struct TileIter {
         }
     }
 
+    // The next plan item into (r, k, n_r, grp, start, count, base); false at
+    // the end of the list or on an item that does not fit (flagged).
+    __device__ bool plan_next() {
+        if (plan_pos >= plan_end) return false;
+        const int32_t *it = plan_items + (int64_t)kPlanItemWords * plan_pos++;
+        const int ir = __ldg(it), w = __ldg(it + 1), s0 = __ldg(it + 2), c = __ldg(it + 3);
+        const int ik = w & 511, inr = (w >> 9) & 511, ig = (w >> 18) & 8191;
+        bool ok = w >= 0 && ir >= 0 && ir < cur.R && inr >= 1 && inr <= cur.num_splits && ik < inr &&
+                  ig < row_groups && s0 >= 0 && c >= 0;
+        if (ok) {
+            const int len = PAGED ? request_len(cur.indptr, ir, cur.num_pages, &base, cur.log2p, cur.last_page_len)
+                                  : request_len(cur.indptr, ir, cur.num_pages, &base);
+            ok = (int64_t)s0 + c <= len;
+        }
+        if (!ok) {
+            flag(MLA_DEV_BAD_PLAN);
+            plan_pos = plan_end;
+            return false;
+        }
+        r = ir; k = ik; n_r = inr; grp = ig; start = s0; count = c;
+        return true;
+    }
+
     __device__ Tile next(int lane) {
         Tile T;
         T.valid = false;
         if (!have_unit || t >= ntiles) {
-            if (plan_ids) {
-                if (plan_pos >= plan_end) {
+            if (plan_items) {
+                if (!plan_next()) {
                     have_unit = false;
                     return T;
                 }
-                const int nu = __ldg(plan_ids + plan_pos++);
-                if (nu <= u) {   // the cursor only walks forward
-                    flag(MLA_DEV_BAD_PLAN);
-                    plan_pos = plan_end;
-                    have_unit = false;
-                    return T;
-                }
-                u = nu;
             } else {
                 u += gridDim.x;
+                int len;
+                if (!cur.find(u / row_groups, lane, &r, &k, &n_r, &len, &base)) {
+                    have_unit = false;
+                    return T;
+                }
+                grp = (int)(u % row_groups);
+                split_range(len, n_r, k, &start, &count);
             }
-            int len;
-            if (!cur.find(u / row_groups, lane, &r, &k, &n_r, &len, &base)) {
-                have_unit = false;
-                return T;
-            }
-            grp = (int)(u % row_groups);
-            split_range(len, n_r, k, &start, &count);
             ntiles = count > 0 ? (count + TILE - 1) / TILE : 1;
             t = 0;
             have_unit = true;

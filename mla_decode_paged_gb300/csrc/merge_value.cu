@@ -15,9 +15,11 @@
 // LSE-merges one latent row straight into smem (lanes own 16 columns, split
 // weights held one per lane, four splits' loads in flight); then warp MMA
 // (bf16, m16n8k16, one 8-column tile per warp) over the 512-wide latent and
-// the gate epilogue.  COLS = 32: four CTAs per row tile, so a small batch
-// still spreads over the SMs (the host routes large batches to the
-// separate merge and value kernels, which read each partial row once).
+// the gate epilogue.  COLS (32, 64 or 128) is the narrowest column block
+// whose grid still fits one wave of one CTA per SM, so a small batch
+// spreads over the SMs without a second wave (the host routes large
+// batches to the separate merge and value kernels, which read each partial
+// row once).
 // Launched with programmatic dependent launch: the W_UV copies and the gate
 // loads (inputs no earlier kernel writes) start while the attend grid is
 // still finishing; griddepcontrol.wait orders every read of the partials
@@ -227,8 +229,14 @@ cudaError_t merge_value_launch(const void *o, const float *lse, int num_splits, 
                                float *lse_out, int sms, cudaStream_t st) {
     const int S = R * qlen;
     if (S == 0) return cudaSuccess;
-    (void)sms;
-    return launch<32>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
+    // One CTA per SM (16 warps, ~94 registers each): the most column blocks
+    // whose grid still fits one wave.
+    const long long tiles = (long long)((S + kRows - 1) / kRows) * H;
+    if (tiles * (MLA_D_V / 32) <= sms)
+        return launch<32>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
+    if (tiles * (MLA_D_V / 64) <= sms)
+        return launch<64>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
+    return launch<128>(o, lse, num_splits, w_uv, gate, lengths, S, qlen, H, out, latent, lse_out, st);
 }
 
 cudaError_t merge_value_status(unsigned int *flags, bool clear) { return read_status(flags, clear); }

@@ -1,6 +1,7 @@
-"""GPU checks of the host work plan (mla_decode_attend_planned): with a plan
-the attend partials are bit-identical to the round-robin launch and match
-the oracle; plans that do not fit the launch are flagged, not faulted."""
+"""GPU checks of the balanced work plan (mla_decode_attend_planned): each
+split's partial matches the oracle over the plan's token range, the merged
+result matches the unsplit oracle, and plans that do not fit the launch are
+flagged, not faulted."""
 
 import numpy as np
 import pytest
@@ -9,8 +10,9 @@ import torch
 import mla_decode_paged_gb300 as mla
 from mla_decode_paged_gb300 import workloads as W
 from oracle import mla_oracle as O
+from tests import _plan
 from tests._bits import bf16_bits, i32, oracle_args, u8
-from tests.parity import assert_bf16_close, assert_lse_close
+from tests.parity import assert_bf16_close, assert_lse_close, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -35,56 +37,90 @@ def _dev(inp):
     return out
 
 
-def _attend(inp, ns, st, plan=None, **kw):
+def _attend(inp, ns, plan=None, st=64, **kw):
     if inp.extra.get("page_size", 1) > 1:
         kw.update(page_size=inp.extra["page_size"], last_page_len=inp.extra["last_page_len"])
     o, lse = mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=inp.heads,
-                        qlen=inp.qlen, plan=plan, **kw)
+                        qlen=inp.qlen, plan=None if plan is None else plan.to(DEV), **kw)
     torch.cuda.synchronize()
     return o, lse
 
 
-def _same(a, b):
-    """Partials equal bit for bit wherever the split is used (finite lse)."""
-    (o1, l1), (o2, l2) = a, b
-    used = torch.isfinite(l1)
-    assert torch.equal(torch.isfinite(l2), used)
-    assert torch.equal(l1[used], l2[used])
-    assert torch.equal(o1[used].view(torch.int16), o2[used].view(torch.int16))
+def _block_args(inp_cpu):
+    if inp_cpu.extra.get("page_size", 1) > 1:
+        return dict(page_size=inp_cpu.extra["page_size"], last_page_len=i32(inp_cpu.extra["last_page_len"]))
+    return {}
 
 
-def _plan(inp_lengths, inp, ns, st):
-    return mla.plan_units(inp_lengths.cpu(), inp.qlen, inp.heads, ns, st).to(DEV)
+def _check_against_oracle(inp_cpu, o, lse, plan, ns, **kw):
+    R = len(i32(inp_cpu.lengths))
+    groups = -(-inp_cpu.qlen * inp_cpu.heads // 48)
+    rg = _plan.ranges(plan, R, 0)
+    for g in range(1, groups):
+        assert _plan.ranges(plan, R, g) == rg
+    a = oracle_args(inp_cpu)
+    ro, rl = O.attend_splits(**a, num_splits=ns, split_tokens=1, ranges=rg, **_block_args(inp_cpu), **kw)
+    assert_lse_close(lse, rl, "planned partial lse")
+    assert_bf16_close(o, ro, "planned partial o", mask=np.isfinite(rl))
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    rlat, rlse = O.attend(**a, **_block_args(inp_cpu), **kw)
+    assert_lse_close(lse_m, rlse, "planned merged lse")
+    assert_bf16_close(latent, rlat, "planned latent")
 
 
-@pytest.mark.parametrize("idx,lengths,ns,st", [
-    (1, [1, 17, 128, 129, 300, 1000], 4, 64),
-    (2, [257, 64, 700], 8, 50),
-    (3, [300, 129], 3, 7),
-    (4, [0, 5, 200, 0, 333], 4, 64),
+@pytest.mark.parametrize("idx,lengths,ns", [
+    (1, [1, 17, 128, 129, 300, 1000], 4),
+    (2, [257, 64, 700], 8),
+    (3, [300, 129], 3),                 # two row groups of 48
+    (4, [0, 5, 200, 0, 333], 4),
+    (1, [5000, 3, 40], 2),              # num_splits binds
 ])
-def test_planned_small_workloads_match_oracle_and_round_robin(idx, lengths, ns, st):
+def test_planned_small_workloads_match_oracle(idx, lengths, ns):
     inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
     inp = _dev(inp_cpu)
-    plan = _plan(inp_cpu.lengths, inp, ns, st)
-    got = _attend(inp, ns, st, plan)
-    _same(got, _attend(inp, ns, st))
-    ro, rl = O.attend_splits(**oracle_args(inp_cpu), num_splits=ns, split_tokens=st)
-    assert_lse_close(got[1], rl, "planned partial lse")
-    assert_bf16_close(got[0], ro, "planned partial o", mask=np.isfinite(rl))
+    plan, used = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, ns)
+    assert used <= ns
+    o, lse = _attend(inp, ns, plan)
+    _check_against_oracle(inp_cpu, o, lse, plan, ns)
+    assert mla.device_status() == 0
+
+
+def test_planned_causal_block_tables_match_oracle():
+    inp_cpu = W.make_block_inputs(2, "cpu", page_size=16, lengths=[2, 3, 257, 700])
+    inp = _dev(inp_cpu)
+    plan, _ = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+    o, lse = _attend(inp, 4, plan, causal=True)
+    _check_against_oracle(inp_cpu, o, lse, plan, 4, causal=True)
+    assert mla.device_status() == 0
+
+
+def test_planned_fp8_query_matches_oracle():
+    inp_cpu = W.make_inputs(1, "cpu", lengths=[1, 17, 128, 129, 300, 1000])
+    inp = _dev(inp_cpu)
+    q8 = (inp_cpu.q.float() * 4).to(torch.float8_e4m3fn)     # codes of q * 4, read with q_scale 1/4
+    plan, _ = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+    o, lse = mla.attend(q8.to(DEV), inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 4, 64, heads=inp.heads,
+                        q_scale=0.25, plan=plan.to(DEV))
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    a = dict(oracle_args(inp_cpu), q_bits=u8(q8.view(torch.uint8)), scale=inp.scale * 0.25)
+    rlat, rlse = O.attend(**a, q_fp8=True)
+    assert_lse_close(lse_m, rlse, "planned fp8-query lse")
+    assert_bf16_close(latent, rlat, "planned fp8-query latent")
     assert mla.device_status() == 0
 
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
 def test_planned_full_size_workloads(idx):
-    """The launch configuration the benchmark times: bit-identical partials,
-    merged output checked against the oracle on sampled requests."""
+    """The launch configuration the benchmark times: merged output checked
+    against the oracle on sampled requests and against the round-robin
+    launch everywhere."""
     inp = W.make_inputs(idx, DEV)
     ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
-    plan = _plan(inp.lengths, inp, ns, st)
-    got = _attend(inp, ns, st, plan)
-    _same(got, _attend(inp, ns, st))
-    latent, lse_m = mla.merge(*got)
+    plan, used = mla.plan_units(inp.lengths.cpu(), inp.qlen, inp.heads, ns)
+    latent, lse_m = mla.merge(*_attend(inp, used, plan))
+    rr_lat, rr_lse = mla.merge(*_attend(inp, ns, st=st))
     torch.cuda.synchronize()
     lens = i32(inp.lengths)
     rng = np.random.default_rng(idx)
@@ -95,78 +131,59 @@ def test_planned_full_size_workloads(idx):
     rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
     assert_lse_close(lse_m[rows], rlse[rows], "planned lse (sampled)")
     assert_bf16_close(latent[rows], rlat[rows], "planned latent (sampled)")
+    # every row: the planned and round-robin launches agree to rounding
+    assert_lse_close(lse_m, to_f64(rr_lse), "planned vs round-robin lse")
+    assert_bf16_close(latent, to_f64(rr_lat), "planned vs round-robin latent")
     assert mla.device_status() == 0
 
 
-def test_planned_block_tables_causal_identical():
-    inp = W.make_block_inputs(2, DEV, page_size=16)
-    ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
-    plan = _plan(inp.lengths, inp, ns, st)
-    _same(_attend(inp, ns, st, plan, causal=True), _attend(inp, ns, st, causal=True))
-    assert mla.device_status() == 0
-
+# ----------------------------------------------------------------- bad plans
 
 def _small():
     inp_cpu = W.make_inputs(1, "cpu", lengths=[1, 17, 128, 129, 300, 1000, 0, 640])
     inp = _dev(inp_cpu)
-    ns, st = 4, 64
-    return inp, ns, st, mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, ns, st)
+    plan, _ = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+    return inp, plan
+
+
+def _first_item(plan):
+    G = int(plan[0])
+    return 2 + G      # word index of item 0 (CTA 0's first item)
+
+
+def _expect_flag(inp, bad):
+    _attend(inp, 4, bad)
+    assert mla.device_status() & mla.DEV_BAD_PLAN
+    assert mla.device_status() == 0
 
 
 def test_plan_for_another_grid_is_flagged():
-    inp, ns, st, plan = _small()
+    inp, plan = _small()
     bad = plan.clone()
     bad[0] += 1
-    _attend(inp, ns, st, bad.to(DEV))
-    assert mla.device_status() & mla.DEV_BAD_PLAN
-    assert mla.device_status() == 0
+    _expect_flag(inp, bad)
 
 
 def test_plan_offsets_outside_the_buffer_are_flagged():
-    inp, ns, st, plan = _small()
+    inp, plan = _small()
     G = int(plan[0])
     bad = plan.clone()
-    bad[1 + G] = plan.numel()        # the last CTA's list runs past the ids
-    _attend(inp, ns, st, bad.to(DEV))
-    assert mla.device_status() & mla.DEV_BAD_PLAN
-    assert mla.device_status() == 0
+    bad[1 + G] = (plan.numel() - 2 - G) // 4 + 1      # the last CTA's list runs past the items
+    _expect_flag(inp, bad)
 
 
-def test_plan_with_decreasing_ids_is_flagged():
-    inp, ns, st, plan = _small()
-    G = int(plan[0])
-    U = plan.numel() - 2 - G
-    assert U <= G
-    # CTA 0 takes units 1 then 0 (decreasing), CTA b > 0 takes unit b + 1
-    counts = [2] + [1] * (U - 2) + [0] * (G - U + 1)
-    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    ids = np.array([1, 0] + list(range(2, U)), dtype=np.int32)
-    bad = torch.from_numpy(np.concatenate([[G], off, ids]).astype(np.int32))
-    assert bad.numel() == plan.numel()
-    _attend(inp, ns, st, bad.to(DEV))
-    assert mla.device_status() & mla.DEV_BAD_PLAN
-    assert mla.device_status() == 0
-
-
-def test_plan_id_past_the_last_unit_ends_that_list():
-    """An id beyond the units ends its CTA's list without a flag; every other
-    unit's partial is still the round-robin one."""
-    inp, ns, st, plan = _small()
-    G = int(plan[0])
-    off = plan[1:G + 2]
-    b = int(np.argmax((off[1:] - off[:-1]).numpy() >= 1))
-    last = G + 2 + int(off[b + 1]) - 1
-    dropped = int(plan[last])
+@pytest.mark.parametrize("field,value", [
+    ("r", 8),            # request past num_requests
+    ("r", -1),
+    ("k", 1 | (1 << 9)),  # k >= n_r
+    ("k", 0 | (5 << 9)),  # n_r > num_splits (4)
+    ("k", 0 | (1 << 9) | (1 << 18)),   # row group past the groups (1)
+    ("start", -128),
+    ("count", 1 << 20),  # past the request's tokens
+])
+def test_plan_items_outside_the_launch_are_flagged(field, value):
+    inp, plan = _small()
+    w = _first_item(plan) + {"r": 0, "k": 1, "start": 2, "count": 3}[field]
     bad = plan.clone()
-    bad[last] = 1 << 30
-    o, lse = _attend(inp, ns, st, bad.to(DEV))
-    assert mla.device_status() == 0
-    ro, rl = _attend(inp, ns, st)
-    # unit ids are (request, split) pairs request-major (one row group here)
-    lens = i32(inp.lengths)
-    pairs = [(r, k) for r, L in enumerate(lens) for k in range(max(1, min(ns, -(-int(L) // st))))]
-    r_d, k_d = pairs[dropped]
-    keep = torch.isfinite(rl)
-    keep[k_d, r_d * inp.qlen:(r_d + 1) * inp.qlen] = False
-    assert torch.equal(lse[keep], rl[keep])
-    assert torch.equal(o[keep].view(torch.int16), ro[keep].view(torch.int16))
+    bad[w] = value
+    _expect_flag(inp, bad)

@@ -1,7 +1,9 @@
-"""Host work plan (mla_plan_units) on the CPU: the plan is a permutation of
-the attend kernel's work units in its numbering, each CTA's list ascending,
-and its busiest CTA within the list-scheduling bound; the planned entry
-point rejects what it can check on the host.  No kernel runs here."""
+"""Host work plan (mla_plan_units) on the CPU: every request's tokens are
+cut into consecutive splits at tile boundaries, each split once per row
+group, the row groups of a request on adjacent CTAs with the same items,
+at most num_splits splits per request, and the busiest CTA within one tile
+of the mean (or of the longest request's share per split); the planned entry point rejects what it can check on the host.
+No kernel runs here."""
 
 import ctypes
 
@@ -10,9 +12,11 @@ import pytest
 import torch
 
 import mla_decode_paged_gb300 as mla
+from tests import _plan
 
 NULL = ctypes.c_void_p(0)
 P16 = ctypes.c_void_p(1 << 20)   # never dereferenced: each case below fails validation first
+TILE, PIECE, EMPTY = 10, 5, 2    # the planner's cost model, tenths of a 128-token tile
 
 
 @pytest.fixture(scope="module")
@@ -21,86 +25,104 @@ def lib():
     return mla.library()
 
 
-def _units(lengths, qlen, heads, ns, st):
-    """Per-unit token counts in the kernels' order: request-major, then
-    split k (the split rule of mla_decode.h), then query-row group."""
-    rows = qlen * heads
-    groups = -(-rows // 48)
-    out = []
-    for L in lengths:
-        L = max(int(L), 0)
-        n = max(1, min(ns, -(-L // st)))
-        b, m = divmod(L, n)
-        for k in range(n):
-            out += [b + (1 if k < m else 0)] * groups
-    return out
+def _groups(qlen, heads):
+    return -(-qlen * heads // 48)
 
 
-def _split(plan):
-    plan = plan.numpy()
-    G = int(plan[0])
-    off = plan[1:G + 2]
-    ids = plan[G + 2:]
-    return G, off, ids
+def _cost(count):
+    return (-(-count // 128)) * TILE + PIECE if count > 0 else EMPTY
 
 
 CASES = [
-    # lengths, qlen, heads, num_splits, split_tokens, G
-    ([5000, 100, 8000, 1, 0, 4096], 1, 12, 7, 1167, 152),
-    (list(range(1, 300)), 1, 12, 4, 64, 152),
-    ([12000] * 32, 1, 96, 7, 4682, 152),             # two row groups of 48
-    ([4000, 9000, 300] * 40, 4, 12, 5, 6543, 148),
-    ([3] * 7, 8, 12, 31, 3992, 8),                   # fewer CTAs than units per request
-    ([], 1, 12, 1, 16, 152),
+    # lengths, qlen, heads, num_splits, G
+    ([5000, 100, 8000, 1, 0, 4096], 1, 12, 7, 152),
+    (list(range(1, 300)), 1, 12, 4, 152),
+    ([12000] * 32, 1, 96, 7, 152),              # two row groups of 48
+    ([4000, 9000, 300] * 40, 4, 12, 5, 148),
+    ([3] * 7, 8, 12, 31, 8),
+    ([], 1, 12, 1, 152),
+    ([70000, 10, 10, 10], 1, 12, 2, 152),       # num_splits binds
 ]
 
 
-@pytest.mark.parametrize("lengths,qlen,heads,ns,st,G", CASES)
-def test_plan_is_a_permutation_in_kernel_numbering(lengths, qlen, heads, ns, st, G):
-    plan = mla.plan_units(lengths, qlen, heads, ns, st, sm_count=G)
-    units = _units(lengths, qlen, heads, ns, st)
-    assert plan.dtype == torch.int32 and plan.numel() == 2 + G + len(units)
-    g, off, ids = _split(plan)
-    assert g == G
-    assert off[0] == 0 and off[-1] == len(units) and np.all(np.diff(off) >= 0)
-    assert sorted(ids.tolist()) == list(range(len(units)))
+@pytest.mark.parametrize("lengths,qlen,heads,ns,G", CASES)
+def test_plan_structure(lengths, qlen, heads, ns, G):
+    plan, used = mla.plan_units(lengths, qlen, heads, ns, sm_count=G)
+    g = _groups(qlen, heads)
+    Gp, off, it = _plan.items(plan)
+    assert Gp == G and plan.dtype == torch.int32
+    assert plan.numel() == 2 + G + _plan.ITEM_WORDS * it.shape[0]
+    assert off[0] == 0 and off[-1] == it.shape[0] and np.all(np.diff(off) >= 0)
+    V = G // g
     for b in range(G):
-        mine = ids[off[b]:off[b + 1]]
-        assert np.all(np.diff(mine) > 0), "CTA %d's units are not ascending" % b
+        mine = it[off[b]:off[b + 1]]
+        if b >= V * g:
+            assert mine.shape[0] == 0
+            continue
+        assert np.all(mine[:, 3] == b % g)                     # row group of the CTA
+        twin = it[off[b - b % g]:off[b - b % g + 1]]            # group 0 of the same virtual CTA
+        assert np.array_equal(np.delete(mine, 3, axis=1), np.delete(twin, 3, axis=1))
+    for grp in range(g):
+        rg = _plan.ranges(plan, len(lengths), grp)
+        for L, cuts in zip(lengths, rg):
+            L = max(L, 0)
+            assert cuts[0][0] == 0 and cuts[-1][1] == L
+            assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
+            assert all(s % 128 == 0 for s, _ in cuts)
+            assert all(e > s for s, e in cuts) or (L == 0 and cuts == [(0, 0)])
+            assert len(cuts) <= ns
+    assert used == max([len(c) for c in _plan.ranges(plan, len(lengths))] or [1])
 
 
-@pytest.mark.parametrize("lengths,qlen,heads,ns,st,G", CASES[:5])
-def test_plan_balance_within_list_scheduling_bound(lengths, qlen, heads, ns, st, G):
-    """Greedy assignment to the least loaded CTA keeps the busiest CTA within
-    mean + the largest unit (Graham's bound); longest-first is never worse
-    than round robin on these length mixes."""
-    units = _units(lengths, qlen, heads, ns, st)
-    cost = [-(-c // 128) + (0.5 if c else 0.2) for c in units]
-    g, off, ids = _split(mla.plan_units(lengths, qlen, heads, ns, st, sm_count=G))
-    load = [sum(cost[i] for i in ids[off[b]:off[b + 1]]) for b in range(G)]
-    assert max(load) <= sum(cost) / G + max(cost) + 1e-9
-    rr = [sum(cost[u] for u in range(b, len(cost), G)) for b in range(G)]
-    assert max(load) <= max(rr) + 1e-9
+@pytest.mark.parametrize("lengths,qlen,heads,ns,G", CASES[:6])
+def test_plan_balance_within_a_tile_of_the_mean(lengths, qlen, heads, ns, G):
+    """The budget is the smallest that fits the grid within num_splits
+    splits per request, so every virtual CTA but the last ends within a tile
+    and a split share of it: the busiest CTA is within that of the larger of
+    the mean and the longest request's share per split."""
+    plan, _ = mla.plan_units(lengths, qlen, heads, ns, sm_count=G)
+    g = _groups(qlen, heads)
+    V = G // g
+    _, off, it = _plan.items(plan)
+    loads = [sum(_cost(c) for c in it[off[v * g]:off[v * g + 1], 5]) for v in range(V)]
+    per_split = max([-(-(-(-L // 128)) // ns) * TILE + PIECE for L in lengths if L > 0] or [0])
+    assert max(loads) <= max(sum(loads) / (V - 1), per_split) + TILE + PIECE
 
 
-def test_plan_example_by_hand():
-    """Three requests of 256, 128 and 1 tokens, one split each, two CTAs:
-    costs 2.5, 1.5, 1.5 -> unit 0 alone on CTA 0, units 1 and 2 on CTA 1."""
-    plan = mla.plan_units([256, 128, 1], 1, 12, 1, 4096, sm_count=2)
-    assert plan.tolist() == [2, 0, 1, 3, 0, 1, 2]
+def test_plan_by_hand_without_cuts():
+    """[256, 128, 1] tokens on 2 CTAs: costs 25, 15, 15; the smallest budget
+    that fits is 30 (request 0 alone, then requests 1 and 2)."""
+    plan, used = mla.plan_units([256, 128, 1], 1, 12, 4, sm_count=2)
+    one = 1 << 9
+    assert plan.tolist() == [2, 0, 1, 3, 0, one, 0, 256, 1, one, 0, 128, 2, one, 0, 1]
+    assert used == 1
+
+
+def test_plan_by_hand_with_cuts():
+    """1000 tokens (8 tiles) on 4 CTAs: budget 25 gives four splits of two
+    tiles; with at most 3 splits the budget grows to 35 (3, 3, 2 tiles)."""
+    plan, used = mla.plan_units([1000], 1, 12, 4, sm_count=4)
+    assert used == 4 and _plan.ranges(plan, 1) == [[(0, 256), (256, 512), (512, 768), (768, 1000)]]
+    plan, used = mla.plan_units([1000], 1, 12, 3, sm_count=4)
+    assert used == 3 and _plan.ranges(plan, 1) == [[(0, 384), (384, 768), (768, 1000)]]
+    _, off, _ = _plan.items(plan)
+    assert off.tolist() == [0, 1, 2, 3, 3]
 
 
 def test_plan_size_query_and_errors(lib):
     lens = torch.tensor([100, 200], dtype=torch.int32)
     lp = ctypes.c_void_p(lens.data_ptr())
-    n = lib.mla_plan_units(2, 1, 12, lp, 4, 64, 10, None, 0)
-    assert n == 2 + 10 + (2 + 4)
+    used = ctypes.c_int(0)
+    n = lib.mla_plan_units(2, 1, 12, lp, 4, 10, None, 0, ctypes.byref(used))
+    assert n == 2 + 10 + 4 * 3 and used.value == 2          # the 2-tile request is cut in two
     buf = torch.empty(n - 1, dtype=torch.int32)
-    assert lib.mla_plan_units(2, 1, 12, lp, 4, 64, 10, ctypes.c_void_p(buf.data_ptr()), n - 1) == mla.MLA_ERR_INVALID
+    assert lib.mla_plan_units(2, 1, 12, lp, 4, 10, ctypes.c_void_p(buf.data_ptr()), n - 1, None) == mla.MLA_ERR_INVALID
     assert b"too small" in lib.mla_last_error()
-    for bad in [(2, 0, 12, lp, 4, 64), (2, 1, 0, lp, 4, 64), (2, 1, 12, lp, 0, 64), (2, 1, 12, lp, 4, 0),
-                (2, 1, 12, NULL, 4, 64), (-1, 1, 12, lp, 4, 64)]:
-        assert lib.mla_plan_units(*bad, 10, None, 0) == mla.MLA_ERR_INVALID
+    for bad in [(2, 0, 12, lp, 4), (2, 1, 0, lp, 4), (2, 1, 12, lp, 0), (2, 1, 12, lp, 257),
+                (2, 1, 12, NULL, 4), (-1, 1, 12, lp, 4)]:
+        assert lib.mla_plan_units(*bad, 10, None, 0, None) == mla.MLA_ERR_INVALID
+    # two row groups need at least two CTAs
+    assert lib.mla_plan_units(2, 1, 96, lp, 4, 1, None, 0, None) == mla.MLA_ERR_UNSUPPORTED
 
 
 def _attend_planned(lib, plan, plan_len, page_size=1, last=NULL):
