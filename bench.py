@@ -282,28 +282,33 @@ def run_gpu(args):
     if mla.device_status():
         raise SystemExit("device status flags after the timed steps")
 
-    # ---- end to end through the public API with host buffers
-    q_h = inp.q.cpu().pin_memory()
-    gate_h = inp.gate.cpu().pin_memory()
-    pages_h = inp.pages.cpu().pin_memory()
-    indptr_h = inp.indptr.cpu().pin_memory()
-    lens_h = inp.lengths.cpu().pin_memory()
-    last_h = last.cpu().pin_memory() if last is not None else None
-    last_d = torch.empty_like(last) if last is not None else None
-    plan_hp = plan_h.pin_memory() if plan_h is not None else None
-    plan_d = torch.empty_like(plan) if plan is not None else None
+    # ---- end to end through the public API with host buffers: the step's
+    # inputs staged in one pinned host buffer and uploaded with one copy
+    # (each piece 256-byte aligned, device views made once), the output read
+    # back with one copy.
+    host_parts = [inp.q, inp.gate, inp.pages, inp.indptr, inp.lengths, last, plan_h]
+    offs, total_b = [], 0
+    for t in host_parts:
+        offs.append(total_b)
+        if t is not None:
+            total_b += (t.numel() * t.element_size() + 255) // 256 * 256
+    stage_h = torch.empty(total_b, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total_b, dtype=torch.uint8, device=dev)
+    views = []
+    for t, off in zip(host_parts, offs):
+        if t is None:
+            views.append(None)
+            continue
+        nb = t.numel() * t.element_size()
+        stage_h[off:off + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        views.append(stage_d[off:off + nb].view(t.dtype).view(t.shape))
+    q_d, gate_d, pages_d, indptr_d, lens_d, last_d, plan_d = views
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d, gate_d = torch.empty_like(inp.q), torch.empty_like(inp.gate)
-    pages_d, indptr_d, lens_d = torch.empty_like(inp.pages), torch.empty_like(inp.indptr), torch.empty_like(inp.lengths)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, gate_h, pages_h, indptr_h, lens_h, last_h, plan_hp)
-              if t is not None)
+    h2d = total_b
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
-        for d, h in ((q_d, q_h), (gate_d, gate_h), (pages_d, pages_h), (indptr_d, indptr_h), (lens_d, lens_h),
-                     (last_d, last_h), (plan_d, plan_hp)):
-            if d is not None:
-                d.copy_(h, non_blocking=True)
+        stage_d.copy_(stage_h, non_blocking=True)
         mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
                    o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, plan=plan_d,
                    stream=stream)
