@@ -96,7 +96,7 @@ def _plan_splits(plan, R):
     return n_r
 
 
-def _plan_stats(inp, ns, st, page_size=1, plan=None):
+def _plan_stats(inp, ns, st, page_size=1, plan=None, q_bytes=2):
     """Host-side split counts and the attend kernel's algorithmic bytes
     (KV rows, page / block indices, indptr, q, partials, the work plan)."""
     lens = inp.lengths.cpu().numpy().astype(np.int64)
@@ -110,7 +110,7 @@ def _plan_stats(inp, ns, st, page_size=1, plan=None):
     total = int(lens.sum())
     R = len(lens)
     index_bytes = 4 * total if page_size == 1 else 4 * int((-(-lens // page_size)).sum()) + 4 * R
-    attend_bytes = (total * 576 + index_bytes + (R + 1) * 4 + R * rows_per_req * 576 * 2 + 4 * plan_len
+    attend_bytes = (total * 576 + index_bytes + (R + 1) * 4 + R * rows_per_req * 576 * q_bytes + 4 * plan_len
                     + used * rows_per_req * (512 * 2 + 4)
                     + int((ns - n_r).sum() + (lens == 0).sum()) * rows_per_req * 4)
     merge_bytes = used * rows_per_req * (512 * 2 + 4) + ns * R * rows_per_req * 4 + R * rows_per_req * (1024 + 4)
@@ -205,7 +205,11 @@ def run_gpu(args):
     if not args.no_plan:
         plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
     plan = None if plan_h is None else plan_h.to(dev)
-    stats = _plan_stats(inp, ns, st, args.page_size, plan_h)
+    # The query: bf16, or (--q-fp8) e4m3 codes of q * 4 read with q_scale 1/4.
+    q_in, q_scale = inp.q, 1.0
+    if args.q_fp8:
+        q_in, q_scale = (inp.q.float() * 4).to(torch.float8_e4m3fn), 0.25
+    stats = _plan_stats(inp, ns, st, args.page_size, plan_h, q_in.element_size())
     stream = torch.cuda.current_stream(dev)
 
     o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
@@ -218,9 +222,9 @@ def run_gpu(args):
     def step(strm, ev=None):
         if ev:
             ev[0].record(strm)
-        mla.attend(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
+        mla.attend(q_in, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
                    o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last, plan=plan,
-                   stream=strm)
+                   q_scale=q_scale, stream=strm)
         if ev:
             ev[1].record(strm)
         if args.three_call:
@@ -286,7 +290,7 @@ def run_gpu(args):
     # inputs staged in one pinned host buffer and uploaded with one copy
     # (each piece 256-byte aligned, device views made once), the output read
     # back with one copy.
-    host_parts = [inp.q, inp.gate, inp.pages, inp.indptr, inp.lengths, last, plan_h]
+    host_parts = [q_in, inp.gate, inp.pages, inp.indptr, inp.lengths, last, plan_h]
     offs, total_b = [], 0
     for t in host_parts:
         offs.append(total_b)
@@ -311,7 +315,7 @@ def run_gpu(args):
         stage_d.copy_(stage_h, non_blocking=True)
         mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
                    o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, plan=plan_d,
-                   stream=stream)
+                   q_scale=q_scale, stream=stream)
         if args.three_call:
             mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=stream)
             mla.value_gate(latent, inp.w_uv, gate_d, lens_d, qlen, out=out, stream=stream)
@@ -366,6 +370,7 @@ def run_gpu(args):
             "parallelism": "replicas" if ws > 1 else "single-gpu",
             "kv": "fp8-e4m3 paged (page size %d%s)" % (args.page_size, ", block tables" if args.page_size > 1 else ""),
             "mask": "causal within a request" if args.causal else "none",
+            "query": "fp8 e4m3 codes of q * 4, q_scale 1/4" if args.q_fp8 else "bf16",
             "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 mma.sync (W_UV)",
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
             "timing": "value: CUDA-graph replay of the step; kernels_us / roofline: eager launches, one event pair each",
@@ -522,6 +527,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--page-size", type=int, default=1,
                     help="KV cache as block tables of this many rows per block (power of two)")
+    ap.add_argument("--q-fp8", action="store_true",
+                    help="fp8 e4m3 query codes (q * 4) with q_scale 1/4 instead of the bf16 query")
     ap.add_argument("--no-plan", action="store_true",
                     help="round-robin work units under the split rule instead of the host work plan")
     ap.add_argument("--causal", action="store_true",

@@ -116,7 +116,8 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
                                      void *o, float *lse, unsigned int flags, const int32_t *plan,
                                      int64_t plan_len, void *stream) {
     if (flags & ~(MLA_ATTEND_CAUSAL | MLA_ATTEND_Q_FP8)) return fail(MLA_ERR_INVALID, "unknown flag bits");
-    if (plan && (plan_len < 3 || !aligned(plan, 4))) return fail(MLA_ERR_INVALID, "plan too short or misaligned");
+    if (plan && (plan_len < 3 || plan_len > INT32_MAX || !aligned(plan, 4)))
+        return fail(MLA_ERR_INVALID, "plan too short, too long or misaligned");
     const bool q8 = (flags & MLA_ATTEND_Q_FP8) != 0;
     int log2p = 0;
     while ((1 << log2p) < page_size && log2p < 9) ++log2p;

@@ -349,8 +349,7 @@ struct TileIter {
     long long u;
     int t, ntiles, start, count, r, k, n_r, base, grp;
     bool have_unit;
-    const int32_t *plan_items;   // null: round robin
-    int plan_pos, plan_end;
+    int plan_pos, plan_end;      // plan_end < 0: round robin
 
     int row_groups;
     __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
@@ -360,11 +359,11 @@ struct TileIter {
         row_groups = groups;
         u = (long long)blockIdx.x - gridDim.x;
         have_unit = false;
-        plan_items = nullptr;
+        plan_pos = 0;
+        plan_end = -1;
         if (plan) {
             // A plan for another grid, or offsets outside the buffer: flagged, no work.
-            plan_items = plan + 2 + gridDim.x;
-            plan_pos = plan_end = 0;
+            plan_end = 0;
             const int64_t items = (plan_len - 2 - (int64_t)gridDim.x) / kPlanItemWords;
             if (plan_len < 2 + (int64_t)gridDim.x || __ldg(plan) != (int)gridDim.x) {
                 flag(MLA_DEV_BAD_PLAN);
@@ -381,9 +380,9 @@ struct TileIter {
 
     // The next plan item into (r, k, n_r, grp, start, count, base); false at
     // the end of the list or on an item that does not fit (flagged).
-    __device__ bool plan_next() {
+    __device__ bool plan_next(const int32_t *plan) {
         if (plan_pos >= plan_end) return false;
-        const int32_t *it = plan_items + (int64_t)kPlanItemWords * plan_pos++;
+        const int32_t *it = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * plan_pos++;
         const int ir = __ldg(it), w = __ldg(it + 1), s0 = __ldg(it + 2), c = __ldg(it + 3);
         const int ik = w & 511, inr = (w >> 9) & 511, ig = (w >> 18) & 8191;
         bool ok = w >= 0 && ir >= 0 && ir < cur.R && inr >= 1 && inr <= cur.num_splits && ik < inr &&
@@ -402,12 +401,13 @@ struct TileIter {
         return true;
     }
 
-    __device__ Tile next(int lane) {
+    // `plan`: the work plan the iterator was initialised with (or null).
+    __device__ Tile next(int lane, const int32_t *plan = nullptr) {
         Tile T;
         T.valid = false;
         if (!have_unit || t >= ntiles) {
-            if (plan_items) {
-                if (!plan_next()) {
+            if (plan_end >= 0) {
+                if (!plan_next(plan)) {
                     have_unit = false;
                     return T;
                 }
