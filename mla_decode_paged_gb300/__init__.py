@@ -29,7 +29,7 @@ MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
 ATTEND_CAUSAL, ATTEND_Q_FP8 = 1, 2
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT, DEV_BAD_PLAN = 1, 2, 4, 8
 
-__all__ = ["attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "plan_units", "debug_gather",
+__all__ = ["Prepared", "attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "plan_units", "debug_gather",
            "kv_append", "device_status", "build", "library", "MlaError"]
 
 
@@ -101,10 +101,40 @@ def _check(status: int, where: str):
         raise MlaError(status, where, library().mla_last_error().decode())
 
 
-def _stream(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device=None) -> int:
     if stream is None:
+        if _raw_stream is not None:   # the current stream's handle without building a Stream object
+            return int(_raw_stream(torch.cuda.current_device() if device is None else device))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Prepared:
+    """A validated call with its arguments marshalled once: calling it
+    launches on ``stream`` (default: the current stream of the tensors'
+    device) with no further checks.  The tensors it was prepared from must
+    stay alive with their shapes and addresses (as for a captured CUDA
+    graph); their contents may change between calls.  ``outputs`` holds what
+    the plain call returns."""
+
+    def __init__(self, fn, args, where, device, outputs, keep):
+        self._fn, self._args, self._where, self._device = fn, args, where, device
+        self.outputs, self._keep = outputs, keep
+
+    def __call__(self, stream=None):
+        st = self._fn(*self._args, ctypes.c_void_p(_stream(stream, self._device)))
+        if st != MLA_OK:
+            _check(st, self._where)
+        return self.outputs
+
+
+def _marshal(fn, args):
+    """Arguments converted to their ctypes types once (None and ctypes
+    instances as they are)."""
+    return [a if a is None or isinstance(a, ctypes._SimpleCData) else t(a) for t, a in zip(fn.argtypes, args)]
 
 
 def _ptr(t):
@@ -124,7 +154,8 @@ def _as_u8(kv: torch.Tensor) -> torch.Tensor:
 
 
 def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
-           o=None, lse=None, causal=False, page_size=1, last_page_len=None, q_scale=1.0, plan=None, stream=None):
+           o=None, lse=None, causal=False, page_size=1, last_page_len=None, q_scale=1.0, plan=None, stream=None,
+           prepare=False):
     """Split-KV attention: returns ``(o [num_splits, S, heads, 512] bf16,
     lse [num_splits, S, heads] f32)``.
 
@@ -141,6 +172,9 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     ``plan``: a device int32 work plan from :func:`plan_units` for the same
     lengths and shape (``mla_decode_attend_planned``): its splits replace
     the ``split_tokens`` rule; the merged result is the same up to rounding.
+    ``prepare=True`` validates and marshals once and returns a
+    :class:`Prepared` call (launch it with ``call(stream)``) instead of
+    launching.
     """
     kv = _as_u8(kv)
     heads = q.shape[1] if heads is None else heads
@@ -166,12 +200,18 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     if plan is not None:
         _need(plan.dtype == torch.int32 and plan.dim() == 1 and plan.is_contiguous() and plan.is_cuda,
               "plan must be a contiguous int32 device tensor")
-    st = library().mla_decode_attend_planned(
-        _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
-        _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
-        heads, float(scale) * float(q_scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o),
-        _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), _ptr(plan),
-        0 if plan is None else plan.numel(), ctypes.c_void_p(_stream(stream)))
+    args = (_ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
+            _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
+            heads, float(scale) * float(q_scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o),
+            _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), _ptr(plan),
+            0 if plan is None else plan.numel())
+    lib = library()
+    if prepare:
+        # marshal once: ctypes converts each argument on every call otherwise
+        conv = _marshal(lib.mla_decode_attend_planned, args)
+        return Prepared(lib.mla_decode_attend_planned, conv, "mla_decode_attend", q.device.index, (o, lse),
+                        (q, kv, pages, indptr, last_page_len, plan))
+    st = lib.mla_decode_attend_planned(*args, ctypes.c_void_p(_stream(stream, q.device.index)))
     _check(st, "mla_decode_attend")
     return o, lse
 
@@ -212,10 +252,11 @@ def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
 
 
 def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=None, lse_out=None,
-                     stream=None):
+                     stream=None, prepare=False):
     """Merge + W_UV + gate in one call (one launch for small batches):
     returns ``out [S, heads*128] bf16``.  ``latent`` (allocated if not given)
-    receives the merged latent, ``lse_out`` (optional) the merged LSE."""
+    receives the merged latent, ``lse_out`` (optional) the merged LSE.
+    ``prepare=True``: a :class:`Prepared` call instead (see :func:`attend`)."""
     _need(o.dtype == torch.bfloat16 and o.dim() == 4 and o.shape[3] == D_LATENT and o.is_contiguous(),
           "o must be contiguous bf16 [splits, S, heads, 512]")
     _need(lse.dtype == torch.float32 and lse.shape == o.shape[:3] and lse.is_contiguous(),
@@ -236,9 +277,14 @@ def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=No
         out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=o.device)
     if latent is None:
         latent = torch.empty((S, H, D_LATENT), dtype=torch.bfloat16, device=o.device)
-    st = library().mla_merge_value_gate(_ptr(o), _ptr(lse), ns, _ptr(w_uv), _ptr(gate), _ptr(lengths),
-                                        lengths.numel(), qlen, H, _ptr(out), _ptr(latent), _ptr(lse_out),
-                                        ctypes.c_void_p(_stream(stream)))
+    args = (_ptr(o), _ptr(lse), ns, _ptr(w_uv), _ptr(gate), _ptr(lengths), lengths.numel(), qlen, H, _ptr(out),
+            _ptr(latent), _ptr(lse_out))
+    lib = library()
+    if prepare:
+        conv = _marshal(lib.mla_merge_value_gate, args)
+        return Prepared(lib.mla_merge_value_gate, conv, "mla_merge_value_gate", o.device.index, out,
+                        (o, lse, w_uv, gate, lengths, out, latent, lse_out))
+    st = lib.mla_merge_value_gate(*args, ctypes.c_void_p(_stream(stream, o.device.index)))
     _check(st, "mla_merge_value_gate")
     return out
 

@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <string>
 #include <algorithm>
+#include <atomic>
 #include <utility>
 #include <vector>
 
@@ -71,9 +72,12 @@ bool use_warp_mma() {
 }
 
 int device_sms() {
+    static std::atomic<int> cached[64] = {};   // per device ordinal; 0: not read yet
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

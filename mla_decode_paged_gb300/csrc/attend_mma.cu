@@ -432,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_mma_kernel(const Params P)
 template <int MT, int TILE>
 cudaError_t launch(const Params &P, int sms, cudaStream_t st) {
     const size_t smem = sizeof(Smem<MT, TILE>);
-    cudaError_t e = cudaFuncSetAttribute(attend_mma_kernel<MT, TILE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_attr_once<attend_mma_kernel<MT, TILE>>((int)smem);
     if (e != cudaSuccess) return e;
     attend_mma_kernel<MT, TILE><<<sms, kThreads, smem, st>>>(P);
     return cudaGetLastError();

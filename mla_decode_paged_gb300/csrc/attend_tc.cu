@@ -285,12 +285,13 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
     }
     int rows[4];
     fetch(cur, rows);
+    // The next tile's descriptor goes into this tile's stage; its rows are
+    // fetched after this tile's copies are issued (so the first copies wait
+    // for one round of index loads, not two).
+    Tile nxt = iter.next(lane, P.plan);
     int n_issued = 0;
     const int rows_total = P.qlen * P.heads;
     for (int it = 0; cur.valid; ++it) {
-        Tile nxt = iter.next(lane, P.plan);
-        int nrows[4];
-        fetch(nxt, nrows);
         // The next unit's query rows into L2 (the softmax converts them when
         // this unit ends).
         if (pw == kProdWarps - 1 && nxt.valid && (nxt.flags & kTileFirst) && nxt.ntok > 0) {
@@ -330,9 +331,9 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
                 tc::gather4(st + C::RopeOff + g8 * 512 + half * 256, mrope, 512, rows[0], rows[1], rows[2], rows[3],
                             &ms.kv_full[s]);
         }
+        fetch(nxt, rows);
         cur = nxt;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rows[i] = nrows[i];
+        if (cur.valid) nxt = iter.next(lane, P.plan);
         n_issued = it + 1;
     }
     // No more work: one last "done" descriptor through the next stage.
@@ -910,8 +911,7 @@ ParamsCausal causal_params(const Params &P) {
 template <int NQ, bool CAUSAL, bool PAGED>
 cudaError_t launch_as(const CUtensorMap &ml, const CUtensorMap &mr, const Params &P, int grid, cudaStream_t st) {
     const size_t smem = smem_bytes<NQ>();
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NQ, CAUSAL, PAGED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_attr_once<attend_tc_kernel<NQ, CAUSAL, PAGED>>((int)smem);
     if (e != cudaSuccess) return e;
     if constexpr (CAUSAL)
         attend_tc_kernel<NQ, CAUSAL, PAGED><<<grid, kThreads, smem, st>>>(ml, mr, causal_params(P));
@@ -946,20 +946,37 @@ cudaError_t attend_tc_launch(const void *q, int64_t q_row_stride, const void *kv
                              int heads, float scale, float kv_scale, int num_splits, int split_tokens, void *o,
                              float *lse, bool causal, int log2p, const int32_t *last_page_len, bool q8,
                              const int32_t *plan, int64_t plan_len, int grid, cudaStream_t st) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap ml, mr;
-    cuuint64_t gdim[2] = {(cuuint64_t)MLA_D_QK, (cuuint64_t)pool_rows};
-    cuuint64_t gstr[1] = {(cuuint64_t)MLA_D_QK};
-    cuuint32_t box_lat[2] = {128, 1}, box_rope[2] = {64, 1}, es[2] = {1, 1};
-    void *base = const_cast<void *>(kv);
-    if (enc(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_lat, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-            CUDA_SUCCESS ||
-        enc(&mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_rope, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-            CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    // The two tensor maps over the KV pool, encoded once per (device, pool)
+    // and reused while a thread keeps launching over the same pool.
+    struct MapCache {
+        int dev;
+        const void *kv;
+        int64_t pool_rows;
+        CUtensorMap ml, mr;
+    };
+    static thread_local MapCache cache = {-1, nullptr, 0, {}, {}};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (cache.dev != dev || cache.kv != kv || cache.pool_rows != pool_rows) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+        if (!enc) return cudaErrorNotSupported;
+        cuuint64_t gdim[2] = {(cuuint64_t)MLA_D_QK, (cuuint64_t)pool_rows};
+        cuuint64_t gstr[1] = {(cuuint64_t)MLA_D_QK};
+        cuuint32_t box_lat[2] = {128, 1}, box_rope[2] = {64, 1}, es[2] = {1, 1};
+        void *base = const_cast<void *>(kv);
+        cache.dev = -1;
+        if (enc(&cache.ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_lat, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&cache.mr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, gdim, gstr, box_rope, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        cache.dev = dev;
+        cache.kv = kv;
+        cache.pool_rows = pool_rows;
+    }
+    const CUtensorMap &ml = cache.ml, &mr = cache.mr;
     Params P;
     P.q = static_cast<const __nv_bfloat16 *>(q);
     P.q_row_stride = q_row_stride;

@@ -3,6 +3,7 @@
 // per-device status word.  Inline PTX for sm_103a.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -18,6 +19,21 @@ namespace mla {
 static __device__ unsigned int g_status;
 
 __device__ __forceinline__ void flag(unsigned int bits) { atomicOr(&g_status, bits); }
+
+// Sets a kernel's dynamic shared-memory limit once per device ordinal
+// (< 64): the runtime call otherwise costs host time on every launch.
+template <auto *KERNEL>
+inline cudaError_t smem_attr_once(int bytes) {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 static inline cudaError_t read_status(unsigned int *flags, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_status, sizeof(unsigned int));

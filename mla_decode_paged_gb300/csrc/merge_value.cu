@@ -204,7 +204,7 @@ cudaError_t launch(const void *o, const float *lse, int num_splits, const void *
                    const int32_t *lengths, int S, int qlen, int H, void *out, void *latent, float *lse_out,
                    cudaStream_t st) {
     const size_t smem = sizeof(Smem<COLS>);
-    cudaError_t e = cudaFuncSetAttribute(merge_value_kernel<COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_attr_once<merge_value_kernel<COLS>>((int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((S + kRows - 1) / kRows, H, MLA_D_V / COLS);

@@ -121,7 +121,7 @@ cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *
     const int S = R * qlen;
     if (S == 0) return cudaSuccess;
     const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(value_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_attr_once<value_gate_kernel>((int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((S + kRows - 1) / kRows, H, MLA_D_V / kCols);
     value_gate_kernel<<<grid, kThreads, smem, st>>>(

@@ -187,3 +187,36 @@ def test_plan_items_outside_the_launch_are_flagged(field, value):
     bad = plan.clone()
     bad[w] = value
     _expect_flag(inp, bad)
+
+
+# ------------------------------------------------------------ prepared calls
+
+def test_prepared_calls_match_plain_calls_and_follow_new_contents():
+    """A prepared attend / merge-value call launches the same work as the
+    plain call, and reads the buffers' current contents at each launch."""
+    inp_cpu = W.make_inputs(1, "cpu", lengths=[1, 17, 128, 129, 300, 1000])
+    inp = _dev(inp_cpu)
+    plan, ns = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+    plan = plan.to(DEV)
+    q = inp.q.clone()
+    o, lse = _attend(inp, ns, plan)
+    ref = mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, inp.qlen)
+    att = mla.attend(q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, 64, heads=inp.heads,
+                     plan=plan, prepare=True)
+    o2, lse2 = att.outputs
+    mv = mla.merge_value_gate(o2, lse2, inp.w_uv, inp.gate, inp.lengths, inp.qlen, prepare=True)
+    att()
+    out = mv()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref) and torch.equal(lse2, lse)
+    # new query contents, same buffers: the prepared calls see them
+    q.mul_(0.5)
+    att()
+    out_half = mv()
+    o3, lse3 = _attend(_dev(W.Inputs(inp_cpu.spec, inp_cpu.q * 0.5, *(getattr(inp_cpu, f) for f in
+                                     ("kv", "pages", "indptr", "lengths", "w_uv", "gate")),
+                                     inp_cpu.scale, inp_cpu.kv_scale)), ns, plan)
+    ref_half = mla.merge_value_gate(o3, lse3, inp.w_uv, inp.gate, inp.lengths, inp.qlen)
+    torch.cuda.synchronize()
+    assert torch.equal(out_half, ref_half) and not torch.equal(out_half, ref)
+    assert mla.device_status() == 0
