@@ -12,8 +12,9 @@
 //
 // Design: one CTA (16 warps) per (16 rows, head, COLS output columns).
 // One warp bulk-copies the CTA's W_UV rows into padded smem while each warp
-// LSE-merges one latent row straight into smem (lanes own 16 columns, split
-// weights held one per lane, four splits' loads in flight); then warp MMA
+// LSE-merges one latent row straight into smem (lanes own 16 columns; the
+// first eight splits' LSE and rows loaded in one round, further splits four
+// at a time); then warp MMA
 // (bf16, m16n8k16, one 8-column tile per warp) over the 512-wide latent and
 // the gate epilogue.  COLS (32, 64 or 128) is the narrowest column block
 // whose grid still fits one wave of one CTA per SM, so a small batch
@@ -52,23 +53,53 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, uint4 v) {
 __device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + expf(-x)); }
 
 // Merged latent row `row` of head h into smem (and optionally global).
+// The first kFirst splits' LSE and partial rows are loaded in one round
+// (rows of unused splits, lse = -inf, are read but never used: their
+// contents are unspecified); any further splits follow four at a time.
+constexpr int kFirst = 8;
+
 __device__ void merge_row(const __nv_bfloat16 *__restrict__ o, const float *__restrict__ lse, int num_splits,
                           long long nrow, long long rowidx, __nv_bfloat16 *dst_smem, __nv_bfloat16 *latent,
                           float *lse_out, int lane) {
+    float lk[kFirst];
+    uint4 f0[kFirst], f1[kFirst];
+#pragma unroll
+    for (int j = 0; j < kFirst; ++j) {
+        lk[j] = -INFINITY;
+        if (j < num_splits) {
+            lk[j] = __ldg(lse + (long long)j * nrow + rowidx);
+            const uint4 *p = reinterpret_cast<const uint4 *>(o + ((long long)j * nrow + rowidx) * MLA_D_LATENT);
+            f0[j] = __ldg(p + lane);
+            f1[j] = __ldg(p + 32 + lane);
+        }
+    }
     float mx = -INFINITY;
-    for (int k = lane; k < num_splits; k += 32) mx = fmaxf(mx, __ldg(lse + (long long)k * nrow + rowidx));
+#pragma unroll
+    for (int j = 0; j < kFirst; ++j) mx = fmaxf(mx, lk[j]);
+    for (int k = kFirst + lane; k < num_splits; k += 32) mx = fmaxf(mx, __ldg(lse + (long long)k * nrow + rowidx));
 #pragma unroll
     for (int d = 16; d; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
     float a0[8], a1[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) a0[e] = a1[e] = 0.f;
+    // Each lane sums the weights of splits lane, lane + 32, ... and the warp
+    // adds the lanes up (the same order as the separate merge kernel, so
+    // both give the same LSE bits).
     float tot = 0.f;
     if (mx > -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < kFirst; ++j)
+            if (lk[j] > -INFINITY) {
+                const float w = expf(lk[j] - mx);
+                if (j == lane) tot += w;
+                fma8(a0, w, f0[j]);
+                fma8(a1, w, f1[j]);
+            }
         for (int kb = 0; kb < num_splits; kb += 32) {
             const int k = kb + lane;
             float w = 0.f;
             bool valid = false;
-            if (k < num_splits) {
+            if (k >= kFirst && k < num_splits) {
                 const float l = __ldg(lse + (long long)k * nrow + rowidx);
                 valid = l > -INFINITY;
                 w = valid ? expf(l - mx) : 0.f;
