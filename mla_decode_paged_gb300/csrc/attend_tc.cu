@@ -558,6 +558,16 @@ __device__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
 // e4m3; lo = 16 * (p - hi)), packed four columns per word.  GUARD maps
 // s = -inf to 0 even where m is still -inf (causal tiles; without the mask
 // every column sees each tile's live tokens, so m is finite by then).
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative
+// error ~2^-22, results below 2^-126 flushed to 0).  p is then rounded to
+// two e4m3 terms (~8 significant bits), so the approximation is invisible
+// next to that rounding.
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int H2, bool GUARD>
 __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)[H2], float (&l)[H2],
                                         uint32_t (&ph)[H2 / 4], uint32_t (&pl)[H2 / 4]) {
@@ -566,7 +576,7 @@ __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)
         float hv[2], lv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2f(sc[j + e] - mr[j + e]) : 0.f;
+            const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2_approx(sc[j + e] - mr[j + e]) : 0.f;
             l[j + e] += pv;
             hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
             lv[e] = (pv - hv[e]) * 16.f;
