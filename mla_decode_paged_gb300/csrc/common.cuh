@@ -283,8 +283,10 @@ struct UnitCursor {
     long long cum_base;
     int n, incl, len, base;
 
+    // `window`: load the first 32 requests' split counts (not needed when a
+    // work plan names the units).
     __device__ void init(const int32_t *ip, int r_count, int64_t pages_len, int ns, int st, int lane,
-                         int lp = 0, const int32_t *last = nullptr) {
+                         int lp = 0, const int32_t *last = nullptr, bool window = true) {
         indptr = ip;
         last_page_len = PAGED ? last : nullptr;
         log2p = PAGED ? lp : 0;
@@ -294,7 +296,7 @@ struct UnitCursor {
         split_tokens = st;
         r_base = 0;
         cum_base = 0;
-        load(lane);
+        if (window) load(lane);
     }
 
     __device__ void load(int lane) {
@@ -371,7 +373,7 @@ struct TileIter {
     __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
                          int groups, int lane, int log2p = 0, const int32_t *last_page_len = nullptr,
                          const int32_t *plan = nullptr, int64_t plan_len = 0) {
-        cur.init(indptr, R, num_pages, num_splits, split_tokens, lane, log2p, last_page_len);
+        cur.init(indptr, R, num_pages, num_splits, split_tokens, lane, log2p, last_page_len, plan == nullptr);
         row_groups = groups;
         u = (long long)blockIdx.x - gridDim.x;
         have_unit = false;
