@@ -220,3 +220,21 @@ def test_prepared_calls_match_plain_calls_and_follow_new_contents():
     torch.cuda.synchronize()
     assert torch.equal(out_half, ref_half) and not torch.equal(out_half, ref)
     assert mla.device_status() == 0
+
+
+@pytest.mark.parametrize("heads,qlen,lengths", [
+    (128, 16, [40, 3, 1]),          # 2048 rows: 43 row groups, 3 virtual CTAs of 43
+    (20, 5, [150, 40, 1, 0, 700]),  # 100 rows: 3 groups of 34 (NQ 48), 50 virtual CTAs
+    (1, 1, [1, 2, 300, 129]),       # a single row
+])
+def test_planned_row_groups_match_oracle(heads, qlen, lengths):
+    """Plans for many and odd row-group counts: every group of a request runs
+    the same items on its own CTA."""
+    spec = W.WorkloadSpec("rows", 11, len(lengths), qlen, heads, heads + (8 if heads < 128 else 0),
+                          "fixed:" + ",".join(map(str, lengths)), 0.7)
+    inp_cpu = W.make_inputs(spec, "cpu", lengths=lengths)
+    inp = _dev(inp_cpu)
+    plan, ns = mla.plan_units(inp_cpu.lengths, qlen, heads, 3)
+    o, lse = _attend(inp, ns, plan)
+    _check_against_oracle(inp_cpu, o, lse, plan, ns)
+    assert mla.device_status() == 0
