@@ -436,7 +436,6 @@ def _ncu_traffic(workload):
     """DRAM bytes per attend launch from the committed ncu summary of this
     workload, if its kernel-source hash matches the current sources (else
     null: the counters describe an older kernel)."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "attend_tc_%s.md" % workload)
     if not os.path.exists(p) or os.environ.get("MLA_ATTEND_KERNEL") == "mma":
         return None
@@ -446,13 +445,24 @@ def _ncu_traffic(workload):
         if ":" in line and line.split(":")[0] in ("kernel_sources_sha256_16", "dram_bytes_per_launch"):
             k, v = line.split(":", 1)
             vals[k] = v.strip()
-    h = hashlib.sha256()
-    for f in ("attend_tc.cu", "tc.cuh", "common.cuh"):
-        with open(os.path.join(ROOT, "mla_decode_paged_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    if vals.get("kernel_sources_sha256_16") != h.hexdigest()[:16]:
+    if vals.get("kernel_sources_sha256_16") != kernel_sources_hash():
         return None
     return int(vals["dram_bytes_per_launch"])
+
+
+def kernel_sources_hash():
+    """First 16 hex digits of the SHA-256 of the attend kernel's sources
+    with comments and whitespace removed (the code the counters describe)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ("attend_tc.cu", "tc.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "mla_decode_paged_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)      # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                     # line comments
+        h.update("".join(src.split()).encode())
+    return h.hexdigest()[:16]
 
 
 def cpu_baseline(spec, inp, budget_s=10.0):

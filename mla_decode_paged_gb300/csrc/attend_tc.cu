@@ -7,31 +7,37 @@
 // scale and kv_scale, partials o [splits, S, H, 512] bf16 and LSE
 // [splits, S, H] f32) and attend (multi-query attention over one latent row
 // per token; padded heads skipped through the row stride).  Same work units
-// and split plan as the warp-MMA kernel.
+// and split rule as the warp-MMA kernel, or the cuts of a host work plan.
 //
-// Design (one persistent CTA per SM, 12 warps):
-//   * warps 5..11 (producers): TMA tile::gather4 copies 4 paged KV rows per
-//     instruction straight into the UMMA canonical layout: the 512 latent
-//     bytes as four 128-byte column blocks with 128B swizzle, the 64 rope
-//     bytes with 64B swizzle.  Rows past the tile's tokens (and bad page
-//     indices) use an out-of-range row, which the TMA fills with zeros.
+// Design (one persistent CTA per SM, 16 warps, 512 threads):
+//   * warps 9..15 (producers): walk the CTA's tiles (units dealt round robin,
+//     or the plan's items) and copy each tile's 128 paged KV rows with TMA
+//     tile::gather4 (4 rows per instruction) straight into the UMMA
+//     canonical layout: the 512 latent bytes as four 128-byte column blocks
+//     with 128B swizzle, the 64 rope bytes with 64B swizzle, two 72 KB
+//     stages.  Rows past the tile's tokens (and bad page indices) use an
+//     out-of-range row, which the TMA fills with zeros.
 //   * The fp8 tile is used as stored (no dequant pass): tokens are the MMA M
 //     dimension (128).  QK^T: S^T[tok, n] = K[tok, :576] . Q'[n, :576]; the
 //     query is split into two e4m3 terms per row, q*2^e = hi + lo/16, stacked
 //     as the B operand's 2*NQ rows, so one MMA chain yields both partial
-//     scores.  P.V: O^T[lat, n] = V^T[lat, tok] . P'^T[tok, n], with the same
-//     smem bytes read MN-major as V^T and P likewise split into hi + lo/16.
+//     scores (an fp8 query is used as one exact term).  P.V:
+//     O^T[lat, n] = V^T[lat, tok] . P'^T[tok, n], with the same smem bytes
+//     read MN-major as V^T and P likewise split into hi + lo/16.
 //     kind::f8f6f4 E4M3 x E4M3 with f32 accumulation in TMEM:
 //     S' at columns [0, 2NQ), O' for latent block b at [2NQ(1+b), 2NQ(2+b)).
-//   * warp 4 (MMA): one thread issues 18 QK MMAs (K = 32 each) and, once P
+//   * warp 8 (MMA): one thread issues 18 QK MMAs (K = 32 each) and, once P
 //     is in smem, 16 PV MMAs per tile; tcgen05.commit releases the stage.
-//   * warps 0..3 (softmax, thread = TMEM lane = token): combine the hi/lo
-//     scores, online softmax in the log2 domain with a lazily updated
-//     reference max (rebased, and O rescaled in TMEM, only when a score
-//     exceeds it by more than 2^8), write P' (hi/lo e4m3) to smem, prepare
-//     the next unit's query, and at a unit's end reduce the row sums and
-//     write o / lse.  With the causal option, column n (query row tq) masks
-//     token positions >= L_r - qlen + tq + 1.
+//   * warps 0..7 (softmax, two warpgroups, thread = TMEM lane = token, each
+//     warpgroup half of the query columns): combine the hi/lo scores, online
+//     softmax in the log2 domain with a lazily updated reference max
+//     (rebased, and O rescaled in TMEM, only when a score exceeds it by more
+//     than 2^8), write P' (hi/lo e4m3) to smem, prepare the next unit's
+//     query, and at a unit's end reduce the row sums and write o / lse.
+//     With the causal option, column n (query row tq) masks token positions
+//     >= L_r - qlen + tq + 1 (a separate instantiation).
+//   * Registers: the softmax warpgroups take 176 (184 causal), the MMA and
+//     producer warpgroups 80 (72) by setmaxnreg.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
