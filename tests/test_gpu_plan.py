@@ -75,6 +75,7 @@ def _check_against_oracle(inp_cpu, o, lse, plan, ns, **kw):
     (3, [300, 129], 3),                 # two row groups of 48
     (4, [0, 5, 200, 0, 333], 4),
     (1, [5000, 3, 40], 2),              # num_splits binds
+    (4, [0, 0, 0], 3),                  # every request empty: lse -inf, latent 0
 ])
 def test_planned_small_workloads_match_oracle(idx, lengths, ns):
     inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
