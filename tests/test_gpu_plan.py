@@ -239,3 +239,58 @@ def test_planned_row_groups_match_oracle(heads, qlen, lengths):
     o, lse = _attend(inp, ns, plan)
     _check_against_oracle(inp_cpu, o, lse, plan, ns)
     assert mla.device_status() == 0
+
+
+def test_all_options_together_match_oracle():
+    """fp8 query, causal mask, block tables of 16 and a work plan in one call."""
+    inp_cpu = W.make_block_inputs(2, "cpu", page_size=16, lengths=[2, 3, 257, 700, 0, 129])
+    inp = _dev(inp_cpu)
+    q8 = (inp_cpu.q.float() * 4).to(torch.float8_e4m3fn)
+    plan, ns = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+    o, lse = mla.attend(q8.to(DEV), inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, 64,
+                        heads=inp.heads, qlen=inp.qlen, q_scale=0.25, causal=True, page_size=16,
+                        last_page_len=inp.extra["last_page_len"], plan=plan.to(DEV))
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    a = dict(oracle_args(inp_cpu), q_bits=u8(q8.view(torch.uint8)), scale=inp.scale * 0.25)
+    blk = _block_args(inp_cpu)
+    ro, rl = O.attend_splits(**a, num_splits=ns, split_tokens=1, ranges=_plan.ranges(plan, 6, 0), causal=True,
+                             q_fp8=True, **blk)
+    assert_lse_close(lse, rl, "all options: partial lse")
+    assert_bf16_close(o, ro, "all options: partial o", mask=np.isfinite(rl))
+    rlat, rlse = O.attend(**a, causal=True, q_fp8=True, **blk)
+    assert_lse_close(lse_m, rlse, "all options: merged lse")
+    assert_bf16_close(latent, rlat, "all options: latent")
+    assert mla.device_status() == 0
+
+
+@pytest.mark.parametrize("planned", [False, True])
+def test_thousands_of_short_requests(planned):
+    """3,000 requests of 0-50 tokens: many 32-request windows of the unit
+    cursor (round robin) or many items per CTA (plan); sampled requests and
+    every empty request checked against the oracle."""
+    g = torch.Generator().manual_seed(21)
+    lengths = torch.randint(0, 51, (3000,), generator=g).tolist()
+    spec = W.WorkloadSpec("many", 12, len(lengths), 1, 12, 12, "fixed:" + ",".join(map(str, lengths)), 0.8)
+    inp_cpu = W.make_inputs(spec, "cpu", lengths=lengths)
+    inp = _dev(inp_cpu)
+    if planned:
+        plan, ns = mla.plan_units(inp_cpu.lengths, 1, 12, 4)
+        o, lse = _attend(inp, ns, plan)
+    else:
+        ns, st = mla.choose_splits(len(lengths), 1, 12, lengths=inp_cpu.lengths)
+        o, lse = _attend(inp, ns, st=st)
+    latent, lse_m = mla.merge(o, lse)
+    torch.cuda.synchronize()
+    lens = np.asarray(lengths)
+    rng = np.random.default_rng(5)
+    reqs = sorted(set(rng.choice(len(lengths), 40, replace=False).tolist()) | {int(np.argmax(lens))})
+    a = dict(q_bits=bf16_bits(inp_cpu.q), kv_codes=u8(inp_cpu.kv), pages=i32(inp_cpu.pages),
+             indptr=i32(inp_cpu.indptr), scale=inp.scale, kv_scale=inp.kv_scale, heads=12, qlen=1)
+    rlat, rlse = O.attend(**a, requests=reqs)
+    assert_lse_close(lse_m[reqs], rlse[reqs], "many requests: lse (sampled)")
+    assert_bf16_close(latent[reqs], rlat[reqs], "many requests: latent (sampled)")
+    empty = torch.from_numpy(lens == 0).to(DEV)
+    assert torch.all(torch.isneginf(lse_m[empty])) and torch.all(latent[empty] == 0)
+    assert torch.isfinite(lse_m[~empty]).all()
+    assert mla.device_status() == 0
