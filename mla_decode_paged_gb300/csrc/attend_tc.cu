@@ -260,6 +260,11 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
     else
         iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, 0, nullptr,
                   P.plan, P.plan_len);
+    // KV rows are read once when each tile has one row group: stream them
+    // through L2 ahead of everything else (the split partials written
+    // meanwhile stay for the merge); with several groups the other CTAs of
+    // a tile re-read it from L2.
+    const uint64_t pol = tc::l2_policy(P.row_groups == 1);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -331,11 +336,11 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
             uint8_t *st = sm + s * C::StageBytes;
             const int g8 = g4 >> 1, half = g4 & 1;
             if (part < 4)
-                tc::gather4(st + part * C::Blk + g8 * 1024 + half * 512, mlat, part * 128, rows[0], rows[1], rows[2],
-                            rows[3], &ms.kv_full[s]);
+                tc::gather4_hint(st + part * C::Blk + g8 * 1024 + half * 512, mlat, part * 128, rows[0], rows[1],
+                                 rows[2], rows[3], &ms.kv_full[s], pol);
             else
-                tc::gather4(st + C::RopeOff + g8 * 512 + half * 256, mrope, 512, rows[0], rows[1], rows[2], rows[3],
-                            &ms.kv_full[s]);
+                tc::gather4_hint(st + C::RopeOff + g8 * 512 + half * 256, mrope, 512, rows[0], rows[1], rows[2],
+                                 rows[3], &ms.kv_full[s], pol);
         }
         fetch(nxt, rows);
         cur = nxt;

@@ -23,6 +23,26 @@ __device__ __forceinline__ void gather4(void *dst, const CUtensorMap *map, int x
         : "memory");
 }
 
+// The same with an L2 cache policy (from l2_policy) for the rows read.
+__device__ __forceinline__ void gather4_hint(void *dst, const CUtensorMap *map, int x, int r0, int r1, int r2,
+                                             int r3, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 cache policy for data read once (evict first) or as usual.
+__device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
+    uint64_t p;
+    if (evict_first)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Swizzle modes of the UMMA shared-memory descriptor.
 constexpr uint32_t kSw128 = 2, kSw64 = 4;
 
