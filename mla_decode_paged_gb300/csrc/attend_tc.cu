@@ -260,11 +260,12 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
     else
         iter.init(P.indptr, P.R, P.num_pages, P.num_splits, P.split_tokens, P.row_groups, lane, 0, nullptr,
                   P.plan, P.plan_len);
-    // KV rows are read once when each tile has one row group: stream them
-    // through L2 ahead of everything else (the split partials written
-    // meanwhile stay for the merge); with several groups the other CTAs of
-    // a tile re-read it from L2.
-    const uint64_t pol = tc::l2_policy(P.row_groups == 1);
+    // KV rows stream through L2 evicted first: the split partials written
+    // meanwhile stay for the merge, and dirty lines left in L2 by earlier
+    // work are not forced out by the stream (with several row groups the
+    // other CTAs of a tile read it at about the same time and still find
+    // it: measured faster for one and for two groups).
+    const uint64_t pol = tc::l2_policy(true);
     auto fetch = [&](const Tile &T, int (&rows)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
