@@ -36,8 +36,8 @@
 //     query, and at a unit's end reduce the row sums and write o / lse.
 //     With the causal option, column n (query row tq) masks token positions
 //     >= L_r - qlen + tq + 1 (a separate instantiation).
-//   * Registers: the softmax warpgroups take 176 (184 causal), the MMA and
-//     producer warpgroups 80 (72) by setmaxnreg.
+//   * Registers: the softmax warpgroups take 176 (184 causal at 48 rows), the
+//     MMA and producer warpgroups 80 (72) by setmaxnreg.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
@@ -867,10 +867,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // it waits for this grid's completion before reading its results.
     asm volatile("griddepcontrol.launch_dependents;");
     // Register split (per warpgroup; 512 x 128 at launch): the two softmax
-    // warpgroups take 176 (184 with the causal mask's extra state), the MMA /
-    // producer warpgroups the rest: 256 x 176 + 256 x 80 = 256 x 184 +
-    // 256 x 72 = 65536.
-    constexpr int kSoftRegs = CAUSAL ? 184 : 176, kRoleRegs = CAUSAL ? 72 : 80;
+    // warpgroups take 176 (184 for the causal mask's extra state at 48 rows),
+    // the MMA / producer warpgroups the rest: 256 x 176 + 256 x 80 =
+    // 256 x 184 + 256 x 72 = 65536.
+    constexpr bool kWideSoft = CAUSAL && NQ == 48;
+    constexpr int kSoftRegs = kWideSoft ? 184 : 176, kRoleRegs = kWideSoft ? 72 : 80;
     static_assert(2 * 128 * (kSoftRegs + kRoleRegs) == 65536, "register split must fill the launch's registers");
     if (warp < kSoftWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
