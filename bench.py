@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -127,10 +128,10 @@ class Clocks:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, directory=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % index)
+        self.path = os.path.join(directory or tempfile.gettempdir(), "mla_bench_clocks_rank%d.csv" % index)
 
     def start(self):
         try:
@@ -255,7 +256,7 @@ def run_gpu(args):
         graph.replay()
     torch.cuda.synchronize(dev)
 
-    clocks = Clocks(local)
+    clocks = Clocks(local, args.clocks_dir)
     clocks.start()
     if ws > 1:
         torch.distributed.barrier()
@@ -549,6 +550,8 @@ def main():
                     help="round-robin work units under the split rule instead of the host work plan")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where the raw nvidia-smi clock samples go (default: the system temp directory)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
