@@ -189,13 +189,14 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
  *   host_lengths  int32 [num_requests], host: tokens per request (<= 0: empty).
  *   num_splits    most splits of one request (the partial buffers' split
  *                 dimension of the attend call that uses the plan).
- *   sm_count      G; <= 0 takes the current device's SM count (the grid the
- *                 attend kernel launches).
+ *   sm_count      G (at most 65536); <= 0 takes the current device's SM
+ *                 count (the grid the attend kernel launches).
  *   plan          int32 [plan_capacity], host, caller-owned; NULL asks for
  *                 the size only.
  *   splits_used   optional out: the most splits any request got (<= num_splits).
  * Returns the plan's length in int32, or a negative mla_status
- * (MLA_ERR_INVALID: bad argument or plan_capacity too small;
+ * (MLA_ERR_INVALID: bad argument, plan_capacity too small or no host
+ * memory for the plan's working lists;
  * MLA_ERR_UNSUPPORTED: fewer SMs than query-row groups).
  */
 #define MLA_PLAN_ITEM_WORDS 4

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <new>
 #include <string>
 #include <algorithm>
 #include <atomic>
@@ -351,12 +352,31 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
 
 }  // namespace
 
+namespace {
+constexpr int kPlanMaxCtas = 65536;
+int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
+                   int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used);
+}  // namespace
+
 int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
                        int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
     if (num_requests < 0 || qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS ||
         num_splits < 1 || num_splits > MLA_MAX_SPLITS || (num_requests > 0 && !host_lengths))
         return fail(MLA_ERR_INVALID, "bad plan arguments");
     if (sm_count <= 0) sm_count = device_sms();
+    if (sm_count > kPlanMaxCtas) return fail(MLA_ERR_INVALID, "sm_count above 65536");
+    try {
+        return plan_build(num_requests, qlen, heads, host_lengths, num_splits, sm_count, plan, plan_capacity,
+                          splits_used);
+    } catch (const std::bad_alloc &) {
+        return fail(MLA_ERR_INVALID, "host memory for the plan");
+    }
+}
+
+namespace {
+
+int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
+                   int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
     int groups, nq;
     mla::attend_tc_shape(qlen * heads, &groups, &nq);
     // Each row group of a request runs on its own CTA; the plan fills
@@ -412,6 +432,8 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
     plan[1 + sm_count] = (int32_t)pos;
     return need;
 }
+
+}  // namespace
 
 mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *k_pe, int64_t k_pe_row_stride,
                          const int64_t *slots, int64_t num_tokens, float k_scale, void *kv, int64_t pool_rows,

@@ -121,6 +121,8 @@ def test_plan_size_query_and_errors(lib):
     for bad in [(2, 0, 12, lp, 4), (2, 1, 0, lp, 4), (2, 1, 12, lp, 0), (2, 1, 12, lp, 257),
                 (2, 1, 12, NULL, 4), (-1, 1, 12, lp, 4)]:
         assert lib.mla_plan_units(*bad, 10, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_plan_units(2, 1, 12, lp, 4, 65537, None, 0, None) == mla.MLA_ERR_INVALID
+    assert b"sm_count" in lib.mla_last_error()
     # two row groups need at least two CTAs
     assert lib.mla_plan_units(2, 1, 96, lp, 4, 1, None, 0, None) == mla.MLA_ERR_UNSUPPORTED
 
