@@ -323,7 +323,8 @@ mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *
  * the partials cost a write and a read.  With host_lengths (int32 [R], host
  * memory, may be NULL) the unit sizes are exact; otherwise they are
  * estimated from max_len and total_len (total_len <= 0: R * max_len).
- * sm_count <= 0 means the current device's SM count.
+ * sm_count <= 0 means the current device's SM count.  qlen outside 1..16,
+ * heads outside 1..128 or sm_count above 65536: returns MLA_ERR_INVALID.
  */
 int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
                       const int32_t *host_lengths, int sm_count, int *split_tokens);

@@ -302,6 +302,8 @@ def choose_splits(num_requests, qlen, heads, max_len=0, total_len=0, sm_count=0,
     ns = library().mla_choose_splits(int(num_requests), int(qlen), int(heads), int(max_len), int(total_len),
                                      None if host is None else ctypes.c_void_p(host.data_ptr()),
                                      int(sm_count), ctypes.byref(st))
+    if ns < 1:
+        _check(ns, "choose_splits")
     return int(ns), int(st.value)
 
 

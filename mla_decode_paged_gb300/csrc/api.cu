@@ -231,8 +231,15 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     return MLA_OK;
 }
 
+namespace {
+// Most CTAs a host split or work plan is made for.
+constexpr int kPlanMaxCtas = 65536;
+}  // namespace
+
 int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
                       const int32_t *host_lengths, int sm_count, int *split_tokens) {
+    if (qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS || sm_count > kPlanMaxCtas)
+        return fail(MLA_ERR_INVALID, "choose_splits: qlen, heads or sm_count out of range");
     if (sm_count <= 0) sm_count = device_sms();
     if (host_lengths) {
         max_len = 0;
@@ -353,7 +360,6 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
 }  // namespace
 
 namespace {
-constexpr int kPlanMaxCtas = 65536;
 int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
                    int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used);
 }  // namespace

@@ -136,6 +136,13 @@ def test_choose_splits_plan_is_valid(R, qlen, H, max_len, total):
     assert 1 <= ns2 <= 256 and -(-max_len // st2) <= ns2
 
 
+@pytest.mark.parametrize("qlen,H,sms", [(0, 12, 152), (17, 12, 152), (1, 0, 152), (1, 129, 152), (1, 12, 65537)])
+def test_choose_splits_rejects_out_of_range_arguments(qlen, H, sms):
+    with pytest.raises(mla.MlaError) as e:
+        mla.choose_splits(4, qlen, H, 1000, 4000, sm_count=sms)
+    assert e.value.status == mla.MLA_ERR_INVALID
+
+
 def _attend_paged(lib, page_size, last=P16, flags=0, **kw):
     a = dict(q=P16, q_row_stride=12 * 576, kv=P16, pool_rows=128, pages=P16, num_pages=10, indptr=P16,
              R=2, qlen=1, heads=12, scale=0.1, kv_scale=1.0, num_splits=4, split_tokens=16, o=P16, lse=P16,
