@@ -375,19 +375,22 @@ def device_status(stream=None) -> int:
 
 
 def decode_step(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, *, heads=None, qlen=1,
-                num_splits=None, split_tokens=None, max_len=None, total_len=0, causal=False, plan=None,
-                stream=None):
-    """The whole step (attend -> merge -> value_gate); returns
+                num_splits=None, split_tokens=None, max_len=None, total_len=0, causal=False, page_size=1,
+                last_page_len=None, q_scale=1.0, plan=None, stream=None):
+    """The whole step (attend, then the merge with value/gate through
+    :func:`merge_value_gate`: one launch for small batches); returns
     ``(out, latent, lse)``.  Without a split plan one is chosen from
-    ``max_len`` (host-known longest request).  ``causal`` and ``plan`` as in
-    :func:`attend`."""
+    ``max_len`` (host-known longest request).  ``causal``, ``page_size``,
+    ``last_page_len``, ``q_scale`` and ``plan`` as in :func:`attend`."""
     heads = q.shape[1] if heads is None else heads
     if num_splits is None or split_tokens is None:
         if max_len is None:
             raise ValueError("give num_splits and split_tokens, or max_len for the split plan")
         num_splits, split_tokens = choose_splits(indptr.numel() - 1, qlen, heads, max_len, total_len)
     o, lse = attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, heads=heads,
-                    qlen=qlen, causal=causal, plan=plan, stream=stream)
-    latent, lse_m = merge(o, lse, stream=stream)
-    out = value_gate(latent, w_uv, gate, lengths, qlen, stream=stream)
+                    qlen=qlen, causal=causal, page_size=page_size, last_page_len=last_page_len,
+                    q_scale=q_scale, plan=plan, stream=stream)
+    lse_m = torch.empty(lse.shape[1:], dtype=torch.float32, device=lse.device)
+    latent = torch.empty(o.shape[1:], dtype=torch.bfloat16, device=o.device)
+    out = merge_value_gate(o, lse, w_uv, gate, lengths, qlen, latent=latent, lse_out=lse_m, stream=stream)
     return out, latent, lse_m

@@ -100,6 +100,22 @@ def test_small_workloads_match_oracle(idx, lengths, plan, kernel):
     assert mla.device_status() == 0
 
 
+@pytest.mark.parametrize("idx,lengths", SMALL)
+def test_decode_step_matches_oracle(idx, lengths):
+    """The one-call step of the public binding (split plan from max_len,
+    attend, then merge + value/gate: one fused launch for these small
+    batches, the two separate kernels for the 96-head one) against the
+    oracle."""
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _to(inp_cpu, DEV)
+    out, latent, lse_m = mla.decode_step(inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, inp.w_uv,
+                                         inp.gate, inp.lengths, heads=inp.heads, qlen=inp.qlen,
+                                         max_len=int(inp_cpu.lengths.max()))
+    torch.cuda.synchronize()
+    _check_full(latent, lse_m, out, inp_cpu)
+    assert mla.device_status() == 0
+
+
 @pytest.mark.parametrize("heads,qlen", [(16, 1), (12, 2), (7, 5), (16, 4), (128, 1), (20, 5), (1, 1), (128, 16)])
 def test_row_counts_and_groups(heads, qlen, kernel):
     """Query-row counts that select each row-tile size and several row groups."""
