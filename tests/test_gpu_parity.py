@@ -142,6 +142,19 @@ def test_peaky_scores(kernel):
     _check_full(latent, lse_m, out, inp_cpu)
 
 
+def test_most_splits(kernel):
+    """num_splits at its cap (256): one request cut into 256 splits of 40
+    tokens (the last ragged), another into 2, a third empty."""
+    inp_cpu = W.make_inputs(1, "cpu", lengths=[256 * 40 - 17, 70, 0])
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 256, 40)
+    assert torch.isfinite(lse[:, 0]).all() and torch.isfinite(lse[:2, 1]).all()
+    assert torch.all(torch.isneginf(lse[2:, 1])) and torch.all(torch.isneginf(lse[:, 2]))
+    _check_partials(o, lse, inp_cpu, 256, 40)
+    _check_full(latent, lse_m, out, inp_cpu)
+    assert mla.device_status() == 0
+
+
 def test_all_requests_empty(kernel):
     inp_cpu = W.make_inputs(4, "cpu", lengths=[0, 0, 0])
     inp = _to(inp_cpu, DEV)
@@ -378,7 +391,9 @@ def _to_blocks(inp, device):
 
 
 @pytest.mark.parametrize("P,idx,lengths", [(2, 4, [0, 5, 200, 0, 333]), (16, 1, [1, 17, 128, 129, 300, 1000]),
-                                           (64, 2, [257, 64, 700]), (16, 3, [300, 129])])
+                                           (64, 2, [257, 64, 700]), (16, 3, [300, 129]),
+                                           (128, 4, [0, 129, 640]),             # a block per tile
+                                           (256, 1, [1, 300, 1000, 256])])      # largest block: tiles share one
 @pytest.mark.parametrize("plan", [(1, 1 << 20), (4, 64), (3, 7)])
 def test_block_table_small_workloads_match_oracle(P, idx, lengths, plan):
     inp_cpu = W.make_block_inputs(idx, "cpu", page_size=P, lengths=lengths)
