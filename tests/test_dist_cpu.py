@@ -27,7 +27,7 @@ def test_two_gloo_ranks_reduce_to_slowest():
     if not dist.is_available():
         pytest.skip("torch.distributed unavailable")
     port = 29500 + os.getpid() % 1000
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:     # no fork of a threaded parent
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
