@@ -190,7 +190,8 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
  *   num_splits    most splits of one request (the partial buffers' split
  *                 dimension of the attend call that uses the plan).
  *   sm_count      G (at most 65536); <= 0 takes the current device's SM
- *                 count (the grid the attend kernel launches).
+ *                 count (the grid the attend kernel launches), and
+ *                 MLA_ERR_CUDA when there is no usable device.
  *   plan          int32 [plan_capacity], host, caller-owned; NULL asks for
  *                 the size only.
  *   splits_used   optional out: the most splits any request got (<= num_splits).
@@ -323,8 +324,9 @@ mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *
  * the partials cost a write and a read.  With host_lengths (int32 [R], host
  * memory, may be NULL) the unit sizes are exact; otherwise they are
  * estimated from max_len and total_len (total_len <= 0: R * max_len).
- * sm_count <= 0 means the current device's SM count.  qlen outside 1..16,
- * heads outside 1..128 or sm_count above 65536: returns MLA_ERR_INVALID.
+ * sm_count <= 0 means the current device's SM count (MLA_ERR_CUDA when
+ * there is no usable device).  qlen outside 1..16, heads outside 1..128 or
+ * sm_count above 65536: returns MLA_ERR_INVALID.
  */
 int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_t total_len,
                       const int32_t *host_lengths, int sm_count, int *split_tokens);

@@ -72,12 +72,20 @@ bool use_warp_mma() {
     return v && std::string(v) == "mma";
 }
 
+// The current device's SM count, or 0 when there is no usable device (the
+// callers then fail with MLA_ERR_CUDA rather than size a grid for a guess).
 int device_sms() {
     static std::atomic<int> cached[64] = {};   // per device ordinal; 0: not read yet
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
     if (dev >= 0 && dev < 64 && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
     if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
@@ -156,14 +164,16 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
     if (q8 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "fp8 query with the warp-MMA kernel");
     if (plan && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "work plan with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int sms = device_sms();
+    if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
     cudaError_t e = use_warp_mma()
                         ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                  num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                 split_tokens, o, lse, device_sms(), st)
+                                                 split_tokens, o, lse, sms, st)
                         : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
                                                 split_tokens, o, lse, causal, log2p, last_page_len, q8, plan,
-                                                plan_len, device_sms(), st);
+                                                plan_len, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return MLA_OK;
 }
@@ -215,6 +225,7 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     if ((int64_t)num_requests * qlen > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int sms = device_sms();
+    if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
     const int64_t S = (int64_t)num_requests * qlen;
     cudaError_t e;
     if (((S + 15) / 16) * heads <= sms / 2) {
@@ -240,7 +251,8 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
                       const int32_t *host_lengths, int sm_count, int *split_tokens) {
     if (qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS || sm_count > kPlanMaxCtas)
         return fail(MLA_ERR_INVALID, "choose_splits: qlen, heads or sm_count out of range");
-    if (sm_count <= 0) sm_count = device_sms();
+    if (sm_count <= 0 && (sm_count = device_sms()) <= 0)
+        return fail(MLA_ERR_CUDA, "choose_splits: no CUDA device to take the SM count from (pass sm_count)");
     if (host_lengths) {
         max_len = 0;
         total_len = 0;
@@ -369,7 +381,8 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
     if (num_requests < 0 || qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS ||
         num_splits < 1 || num_splits > MLA_MAX_SPLITS || (num_requests > 0 && !host_lengths))
         return fail(MLA_ERR_INVALID, "bad plan arguments");
-    if (sm_count <= 0) sm_count = device_sms();
+    if (sm_count <= 0 && (sm_count = device_sms()) <= 0)
+        return fail(MLA_ERR_CUDA, "plan_units: no CUDA device to take the SM count from (pass sm_count)");
     if (sm_count > kPlanMaxCtas) return fail(MLA_ERR_INVALID, "sm_count above 65536");
     try {
         return plan_build(num_requests, qlen, heads, host_lengths, num_splits, sm_count, plan, plan_capacity,
@@ -455,8 +468,10 @@ mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *
     if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(kv, 16) || !aligned(slots, 8))
         return fail(MLA_ERR_INVALID, "misaligned pointer (kv_c, k_pe, kv need 16 bytes, slots 8)");
     if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    const int sms = device_sms();
+    if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
     cudaError_t e = mla::kv_append_launch(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slots, num_tokens, k_scale,
-                                          kv, pool_rows, device_sms(), static_cast<cudaStream_t>(stream));
+                                          kv, pool_rows, sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
     return MLA_OK;
 }

@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import mla_decode_paged_gb300 as mla
 
@@ -141,6 +142,19 @@ def test_choose_splits_rejects_out_of_range_arguments(qlen, H, sms):
     with pytest.raises(mla.MlaError) as e:
         mla.choose_splits(4, qlen, H, 1000, 4000, sm_count=sms)
     assert e.value.status == mla.MLA_ERR_INVALID
+
+
+def test_sm_count_from_a_missing_device_is_an_error(lib):
+    """Without a device the host plans cannot take the SM count from it:
+    they fail instead of sizing for a guessed grid."""
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(mla.MlaError) as e:
+        mla.choose_splits(4, 1, 12, 1000, 4000)
+    assert e.value.status == mla.MLA_ERR_CUDA
+    lens = torch.tensor([100, 200], dtype=torch.int32)
+    assert lib.mla_plan_units(2, 1, 12, ctypes.c_void_p(lens.data_ptr()), 4, 0, None, 0, None) == mla.MLA_ERR_CUDA
+    assert b"sm_count" in lib.mla_last_error()
 
 
 def _attend_paged(lib, page_size, last=P16, flags=0, **kw):
