@@ -146,6 +146,22 @@ def _need(cond: bool, msg: str):
         raise ValueError(msg)
 
 
+def _same_device(dev, **named):
+    """Every given tensor lives on the CUDA device ``dev``: a host pointer or
+    another device's pointer handed to a kernel would fault."""
+    _need(dev.type == "cuda", "tensors must be CUDA tensors (got %s)" % dev)
+    for name, t in named.items():
+        if t is not None:
+            _need(t.device == dev, "%s is on %s, expected %s" % (name, t.device, dev))
+
+
+def _buffer(t, name, dtype, shape):
+    """A caller-supplied output: exactly this dtype and shape, contiguous
+    (the kernels write every element of that extent)."""
+    _need(t.dtype == dtype and tuple(t.shape) == tuple(shape) and t.is_contiguous(),
+          "%s must be a contiguous %s tensor of shape %s" % (name, dtype, list(shape)))
+
+
 def _as_u8(kv: torch.Tensor) -> torch.Tensor:
     if kv.dtype == torch.float8_e4m3fn:
         kv = kv.view(torch.uint8)
@@ -190,15 +206,21 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
     _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
     _need(pages.dtype == torch.int32 and indptr.dtype == torch.int32, "pages / indptr must be int32")
     _need(pages.is_contiguous() and indptr.is_contiguous(), "pages / indptr must be contiguous")
+    _same_device(q.device, kv=kv, pages=pages, indptr=indptr, o=o, lse=lse, plan=plan,
+                 last_page_len=last_page_len if page_size > 1 else None)
     if o is None:
         o = torch.empty((num_splits, S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    else:
+        _buffer(o, "o", torch.bfloat16, (num_splits, S, heads, D_LATENT))
     if lse is None:
         lse = torch.empty((num_splits, S, heads), dtype=torch.float32, device=q.device)
+    else:
+        _buffer(lse, "lse", torch.float32, (num_splits, S, heads))
     if page_size > 1:
         _need(last_page_len is not None and last_page_len.dtype == torch.int32 and last_page_len.numel() == R
               and last_page_len.is_contiguous(), "page_size > 1 needs last_page_len int32 [R]")
     if plan is not None:
-        _need(plan.dtype == torch.int32 and plan.dim() == 1 and plan.is_contiguous() and plan.is_cuda,
+        _need(plan.dtype == torch.int32 and plan.dim() == 1 and plan.is_contiguous(),
               "plan must be a contiguous int32 device tensor")
     args = (_ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
             _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
@@ -223,12 +245,17 @@ def merge(o, lse, *, latent=None, lse_out=None, want_lse=True, stream=None):
     _need(lse.dtype == torch.float32 and lse.shape == o.shape[:3] and lse.is_contiguous(),
           "lse must be contiguous f32 [splits, S, heads]")
     ns, S, H = o.shape[:3]
+    _same_device(o.device, lse=lse, latent=latent, lse_out=lse_out)
     if latent is None:
         latent = torch.empty((S, H, D_LATENT), dtype=torch.bfloat16, device=o.device)
+    else:
+        _buffer(latent, "latent", torch.bfloat16, (S, H, D_LATENT))
     if lse_out is None and want_lse:
         lse_out = torch.empty((S, H), dtype=torch.float32, device=o.device)
+    elif lse_out is not None:
+        _buffer(lse_out, "lse_out", torch.float32, (S, H))
     st = library().mla_merge_splits(_ptr(o), _ptr(lse), ns, S, H, _ptr(latent), _ptr(lse_out),
-                                    ctypes.c_void_p(_stream(stream)))
+                                    ctypes.c_void_p(_stream(stream, o.device.index)))
     _check(st, "mla_merge_splits")
     return latent, lse_out
 
@@ -242,11 +269,15 @@ def value_gate(latent, w_uv, gate, lengths, qlen=1, *, out=None, stream=None):
           "w_uv must be contiguous bf16 [heads, 128, 512]")
     _need(gate.dtype == torch.bfloat16 and tuple(gate.shape) == (S, H * D_V) and gate.is_contiguous(),
           "gate must be contiguous bf16 [S, heads*128]")
-    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S, "lengths must be int32 [S / qlen]")
+    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S and lengths.is_contiguous(),
+          "lengths must be contiguous int32 [S / qlen]")
+    _same_device(latent.device, w_uv=w_uv, gate=gate, lengths=lengths, out=out)
     if out is None:
         out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=latent.device)
+    else:
+        _buffer(out, "out", torch.bfloat16, (S, H * D_V))
     st = library().mla_value_gate(_ptr(latent), _ptr(w_uv), _ptr(gate), _ptr(lengths), lengths.numel(), qlen,
-                                  H, _ptr(out), ctypes.c_void_p(_stream(stream)))
+                                  H, _ptr(out), ctypes.c_void_p(_stream(stream, latent.device.index)))
     _check(st, "mla_value_gate")
     return out
 
@@ -266,15 +297,17 @@ def merge_value_gate(o, lse, w_uv, gate, lengths, qlen=1, *, out=None, latent=No
           "w_uv must be contiguous bf16 [heads, 128, 512]")
     _need(gate.dtype == torch.bfloat16 and tuple(gate.shape) == (S, H * D_V) and gate.is_contiguous(),
           "gate must be contiguous bf16 [S, heads*128]")
-    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S, "lengths must be int32 [S / qlen]")
+    _need(lengths.dtype == torch.int32 and lengths.numel() * qlen == S and lengths.is_contiguous(),
+          "lengths must be contiguous int32 [S / qlen]")
+    _same_device(o.device, lse=lse, w_uv=w_uv, gate=gate, lengths=lengths, out=out, latent=latent, lse_out=lse_out)
     if latent is not None:
-        _need(latent.dtype == torch.bfloat16 and tuple(latent.shape) == (S, H, D_LATENT) and latent.is_contiguous(),
-              "latent must be contiguous bf16 [S, heads, 512]")
+        _buffer(latent, "latent", torch.bfloat16, (S, H, D_LATENT))
     if lse_out is not None:
-        _need(lse_out.dtype == torch.float32 and tuple(lse_out.shape) == (S, H) and lse_out.is_contiguous(),
-              "lse_out must be contiguous f32 [S, heads]")
+        _buffer(lse_out, "lse_out", torch.float32, (S, H))
     if out is None:
         out = torch.empty((S, H * D_V), dtype=torch.bfloat16, device=o.device)
+    else:
+        _buffer(out, "out", torch.bfloat16, (S, H * D_V))
     if latent is None:
         latent = torch.empty((S, H, D_LATENT), dtype=torch.bfloat16, device=o.device)
     args = (_ptr(o), _ptr(lse), ns, _ptr(w_uv), _ptr(gate), _ptr(lengths), lengths.numel(), qlen, H, _ptr(out),
@@ -333,11 +366,16 @@ def debug_gather(kv, pages, indptr, total_rows=None, stream=None):
     """Every request's KV rows in request order ([sum L, 576] uint8), gathered
     by the attend kernels' own row addressing."""
     kv = _as_u8(kv)
+    _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
+    _need(pages.dtype == torch.int32 and indptr.dtype == torch.int32 and pages.is_contiguous()
+          and indptr.is_contiguous(), "pages / indptr must be contiguous int32")
+    _same_device(kv.device, pages=pages, indptr=indptr)
     if total_rows is None:
         total_rows = int(indptr[-1].item())
     out = torch.empty((total_rows, D_QK), dtype=torch.uint8, device=kv.device)
     st = library().mla_debug_gather(_ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
-                                    indptr.numel() - 1, total_rows, _ptr(out), ctypes.c_void_p(_stream(stream)))
+                                    indptr.numel() - 1, total_rows, _ptr(out),
+                                    ctypes.c_void_p(_stream(stream, kv.device.index)))
     _check(st, "mla_debug_gather")
     return out
 
@@ -359,8 +397,10 @@ def kv_append(kv, kv_c, k_pe, slots, k_scale, *, stream=None):
     T = kv_c.shape[0]
     _need(k_pe.shape[0] == T and slots.dtype == torch.int64 and slots.numel() == T and slots.is_contiguous(),
           "slots must be contiguous int64 [T] matching kv_c / k_pe")
+    _same_device(kvu.device, kv_c=kv_c, k_pe=k_pe, slots=slots)
     st = library().mla_kv_append(_ptr(kv_c), kv_c.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(slots), T,
-                                 float(k_scale), _ptr(kvu), kvu.shape[0], ctypes.c_void_p(_stream(stream)))
+                                 float(k_scale), _ptr(kvu), kvu.shape[0],
+                                 ctypes.c_void_p(_stream(stream, kvu.device.index)))
     _check(st, "mla_kv_append")
     return kv
 

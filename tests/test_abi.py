@@ -144,6 +144,30 @@ def test_choose_splits_rejects_out_of_range_arguments(qlen, H, sms):
     assert e.value.status == mla.MLA_ERR_INVALID
 
 
+def test_binding_rejects_host_tensors_before_any_launch():
+    """Host tensors (whose pointers a kernel would fault on) and tensors on
+    another device are refused in the binding."""
+    q = torch.zeros(2, 12, 576, dtype=torch.bfloat16)
+    kv = torch.zeros(8, 576, dtype=torch.uint8)
+    pages = torch.zeros(4, dtype=torch.int32)
+    indptr = torch.tensor([0, 2, 4], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        mla.attend(q, kv, pages, indptr, 0.1, 1.0, 2, 16)
+    o = torch.zeros(2, 2, 12, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        mla.merge(o, torch.zeros(2, 2, 12))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        mla.kv_append(kv, torch.zeros(1, 512, dtype=torch.bfloat16), torch.zeros(1, 64, dtype=torch.bfloat16),
+                      torch.zeros(1, dtype=torch.int64), 1.0)
+    with pytest.raises(ValueError, match="gate is on cpu"):
+        mla._same_device(torch.device("cuda", 0), gate=torch.zeros(1))
+    with pytest.raises(ValueError, match="o must be a contiguous"):
+        mla._buffer(torch.zeros(2, 3), "o", torch.float32, (3, 2))
+    with pytest.raises(ValueError, match="o must be a contiguous"):
+        mla._buffer(torch.zeros(3, 2).t(), "o", torch.float32, (2, 3))
+    mla._buffer(torch.zeros(2, 3), "o", torch.float32, (2, 3))
+
+
 def test_sm_count_from_a_missing_device_is_an_error(lib):
     """Without a device the host plans cannot take the SM count from it:
     they fail instead of sizing for a guessed grid."""

@@ -155,6 +155,28 @@ def test_most_splits(kernel):
     assert mla.device_status() == 0
 
 
+def test_caller_buffers_of_the_wrong_extent_are_refused():
+    """Outputs the caller supplies must match the call's extent exactly:
+    a smaller one would be written past its end."""
+    inp = _to(W.make_inputs(0, "cpu"), DEV)
+    args = (inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, 4, 25)
+    small_o = torch.empty(3, 2, 12, 512, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError, match="o must be"):
+        mla.attend(*args, heads=12, o=small_o)
+    with pytest.raises(ValueError, match="lse must be"):
+        mla.attend(*args, heads=12, lse=torch.empty(4, 2, 11, device=DEV))
+    o, lse = mla.attend(*args, heads=12)
+    with pytest.raises(ValueError, match="latent must be"):
+        mla.merge(o, lse, latent=torch.empty(2, 12, 256, dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError, match="out must be"):
+        mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, out=torch.empty(2, 1000, dtype=torch.bfloat16,
+                                                                                        device=DEV))
+    with pytest.raises(ValueError, match="CUDA tensors|is on cpu"):
+        mla.merge_value_gate(o, lse, inp.w_uv, inp.gate.cpu(), inp.lengths)
+    torch.cuda.synchronize()
+    assert mla.device_status() == 0
+
+
 def test_all_requests_empty(kernel):
     inp_cpu = W.make_inputs(4, "cpu", lengths=[0, 0, 0])
     inp = _to(inp_cpu, DEV)
