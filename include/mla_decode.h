@@ -342,6 +342,18 @@ mla_status mla_debug_gather(const void *kv, int64_t pool_rows, const int32_t *pa
                             int64_t total_rows, void *out, void *stream);
 
 /*
+ * mla_debug_wait_timeout -- test hook for the device-side failure path (no
+ * counterpart on the pages: it belongs to this library's error handling).
+ * Enqueues one 32-thread CTA whose first thread waits, through the same
+ * bounded mbarrier wait every kernel here uses, on a barrier that nothing
+ * arrives at.  After the wait budget (4e9 SM cycles, about 2 s at 2 GHz) it
+ * sets MLA_DEV_TIMEOUT and returns: the context stays usable and nothing is
+ * left in flight.  Returns MLA_ERR_CUDA without a device or if the launch
+ * fails.
+ */
+mla_status mla_debug_wait_timeout(void *stream);
+
+/*
  * mla_device_status -- synchronises `stream`, returns the current device's
  * status word (MLA_DEV_* bits set by kernels since the last read) in
  * *flags and clears it.  Returns MLA_ERR_CUDA if the synchronisation fails.

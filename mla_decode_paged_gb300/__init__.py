@@ -30,6 +30,7 @@ ATTEND_CAUSAL, ATTEND_Q_FP8 = 1, 2
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT, DEV_BAD_PLAN = 1, 2, 4, 8
 
 __all__ = ["Prepared", "attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "plan_units", "debug_gather",
+           "debug_wait_timeout",
            "kv_append", "device_status", "build", "library", "MlaError"]
 
 
@@ -77,9 +78,10 @@ def library() -> ctypes.CDLL:
     lib.mla_choose_splits.argtypes = [i32, i32, i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mla_debug_gather.argtypes = [vp, i64, vp, i64, vp, i32, i64, vp, vp]
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.mla_debug_wait_timeout.argtypes = [vp]
     lib.mla_kv_append.argtypes = [vp, i64, vp, i64, vp, i64, f32, vp, i64, vp]
     for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_decode_attend_planned", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
-                 "mla_device_status", "mla_choose_splits", "mla_kv_append"):
+                 "mla_device_status", "mla_choose_splits", "mla_kv_append", "mla_debug_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -403,6 +405,12 @@ def kv_append(kv, kv_c, k_pe, slots, k_scale, *, stream=None):
                                  ctypes.c_void_p(_stream(stream, kvu.device.index)))
     _check(st, "mla_kv_append")
     return kv
+
+
+def debug_wait_timeout(stream=None):
+    """Test hook: enqueue a kernel whose bounded wait runs out (about 2 s);
+    it sets DEV_TIMEOUT, which :func:`device_status` then reports."""
+    _check(library().mla_debug_wait_timeout(ctypes.c_void_p(_stream(stream))), "mla_debug_wait_timeout")
 
 
 def device_status(stream=None) -> int:

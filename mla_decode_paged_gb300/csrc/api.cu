@@ -42,6 +42,7 @@ cudaError_t merge_value_status(unsigned int *flags, bool clear);
 cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
                           int R, int64_t total_rows, void *out, cudaStream_t st);
 cudaError_t gather_status(unsigned int *flags, bool clear);
+cudaError_t stuck_wait_launch(cudaStream_t st);
 cudaError_t kv_append_launch(const void *kv_c, int64_t kv_c_stride, const void *k_pe, int64_t k_pe_stride,
                              const int64_t *slots, int64_t T, float k_scale, void *kv, int64_t pool_rows, int sms,
                              cudaStream_t st);
@@ -473,6 +474,13 @@ mla_status mla_kv_append(const void *kv_c, int64_t kv_c_row_stride, const void *
     cudaError_t e = mla::kv_append_launch(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slots, num_tokens, k_scale,
                                           kv, pool_rows, sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return MLA_OK;
+}
+
+mla_status mla_debug_wait_timeout(void *stream) {
+    if (device_sms() <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
+    cudaError_t e = mla::stuck_wait_launch(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait-timeout launch");
     return MLA_OK;
 }
 

@@ -39,7 +39,25 @@ __global__ void __launch_bounds__(32) gather_kernel(const uint8_t *__restrict__ 
     }
 }
 
+// One thread waits, through the kernels' own bounded wait (mbar_wait), on
+// an mbarrier that nothing arrives at and no copy completes: after the wait
+// budget it flags MLA_DEV_TIMEOUT and the kernel returns.  Nothing is in
+// flight when it exits.
+__global__ void __launch_bounds__(32) stuck_wait_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        mbar_wait(&bar, 0);
+    }
+}
+
 }  // namespace
+
+cudaError_t stuck_wait_launch(cudaStream_t st) {
+    stuck_wait_kernel<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
+}
 
 cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
                           int R, int64_t total_rows, void *out, cudaStream_t st) {

@@ -7,6 +7,7 @@ configuration the benchmark times (split plan from mla_choose_splits) and
 are checked on sampled requests the oracle computes one by one."""
 
 import math
+import time
 
 import numpy as np
 import pytest
@@ -294,6 +295,22 @@ def test_bad_pages_and_indptr_are_flagged_not_faulted(kernel):
     bad_ip[1] = bad_ip[2] + 1             # decreasing: request treated as empty + flagged
     mla.attend(inp.q, inp.kv, inp.pages, bad_ip, inp.scale, inp.kv_scale, 1, 1 << 20)
     assert mla.device_status() & mla.DEV_BAD_INDPTR
+    assert mla.device_status() == 0
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_survives():
+    """A kernel waits, through the bounded wait every kernel here uses, on a
+    barrier nothing completes: it gives up after its budget (~2 s), flags
+    DEV_TIMEOUT and exits; the next step on the same context is exact."""
+    assert mla.device_status() == 0
+    t0 = time.time()
+    mla.debug_wait_timeout()
+    assert mla.device_status() & mla.DEV_TIMEOUT
+    assert time.time() - t0 < 60
+    inp_cpu = W.make_inputs(0, "cpu")
+    inp = _to(inp_cpu, DEV)
+    o, lse, latent, lse_m, out = _run_path(inp, 4, 25)
+    _check_full(latent, lse_m, out, inp_cpu)
     assert mla.device_status() == 0
 
 
