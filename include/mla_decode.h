@@ -217,8 +217,9 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
  * another grid, offsets outside the buffer, or an item outside the launch
  * (r >= num_requests, k >= n_r, n_r > num_splits, group >= the row groups,
  * a range past the request's tokens) sets MLA_DEV_BAD_PLAN and ends that
- * CTA's list, leaving its remaining splits unwritten.  plan_len < 3 with a
- * plan: MLA_ERR_INVALID; a plan with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
+ * CTA's list, leaving its remaining splits unwritten.  A plan with plan_len
+ * < 3 or > 2^31 - 1, or not 4-byte aligned: MLA_ERR_INVALID; a plan with the
+ * warp-MMA kernel: MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv,
                                      int64_t pool_rows, const int32_t *pages, int64_t num_pages,
