@@ -366,7 +366,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3x2-f32acc (q and P as two e4m3 terms; bf16 W_UV)",
+        "dtype": "e4m3",    # the attend MMAs (f32 accumulation; config.mma has the rest)
         "data": "synthetic",
         "config": {
             "workload": spec.name, "requests": R, "qlen": qlen, "heads": H, "rows": S,
