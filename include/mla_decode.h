@@ -361,6 +361,48 @@ mla_status mla_debug_wait_timeout(void *stream);
  */
 mla_status mla_device_status(void *stream, unsigned int *flags);
 
+/*
+ * mla_decode_step_static -- one whole decode step that allocates nothing.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory while they run -- a serving loop whose
+ * memory is planned up front and may not grow, a plain C host with no
+ * device allocator, code that must not stall on cudaMalloc's implicit
+ * synchronisation.  Such callers can hold the step's inputs and outputs,
+ * but not the split partials that pass from attend to the merge.  Here
+ * those partials live in one buffer inside the library, a static device
+ * array of MLA_STATIC_SCRATCH_BYTES (32 MiB) that every GPU loading the
+ * library keeps until the process exits.
+ *
+ * It runs mla_decode_attend_planned (page size 1, bf16 query, no flags)
+ * into that buffer and then mla_merge_value_gate from it, so its results
+ * are those of the two calls with caller-owned partials.  Arguments as
+ * those two calls (plan may be NULL: round robin under the split rule;
+ * latent is required, lse_out may be NULL).
+ *
+ *   - Size limit: the partials need num_splits * S * heads * 1028 bytes
+ *     (plus up to 255 bytes of alignment); above MLA_STATIC_SCRATCH_BYTES
+ *     the call returns MLA_ERR_UNSUPPORTED before launching anything, and
+ *     mla_last_error() gives the size needed.
+ *   - Allocation: none (no cudaMalloc, cudaFree or allocating library
+ *     routine).  The first call on a device looks up the buffer's device
+ *     address (cudaGetSymbolAddress, which also loads the library's module
+ *     there); make that first call before any stream capture.
+ *   - Sharing: every call uses the same buffer and leaves its partials in
+ *     it.  Nothing in it has to start at zero (attend writes every LSE of
+ *     the launch, -inf for unused splits, and the merge reads a partial row
+ *     only where its LSE is finite), but two calls whose kernels overlap on
+ *     the GPU (different streams without ordering, or several host threads)
+ *     race on it: order them on one stream.
+ */
+#define MLA_STATIC_SCRATCH_BYTES 33554432 /* 32 MiB */
+mla_status mla_decode_step_static(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                  const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                                  int num_requests, int qlen, int heads, float scale, float kv_scale,
+                                  int num_splits, int split_tokens, const int32_t *plan, int64_t plan_len,
+                                  const void *w_uv, const void *gate, const int32_t *lengths, void *out,
+                                  void *latent, float *lse_out, void *stream);
+
 /* Static description of a status code. */
 const char *mla_status_string(mla_status status);
 

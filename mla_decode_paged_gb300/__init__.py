@@ -28,8 +28,10 @@ D_QK, D_LATENT, D_V = 576, 512, 128
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
 ATTEND_CAUSAL, ATTEND_Q_FP8 = 1, 2
 DEV_BAD_PAGE, DEV_BAD_INDPTR, DEV_TIMEOUT, DEV_BAD_PLAN = 1, 2, 4, 8
+STATIC_SCRATCH_BYTES = 32 << 20   # MLA_STATIC_SCRATCH_BYTES: the partials buffer of decode_step_static
 
-__all__ = ["Prepared", "attend", "merge", "value_gate", "merge_value_gate", "decode_step", "choose_splits", "plan_units", "debug_gather",
+__all__ = ["Prepared", "attend", "merge", "value_gate", "merge_value_gate", "decode_step", "decode_step_static",
+           "STATIC_SCRATCH_BYTES", "choose_splits", "plan_units", "debug_gather",
            "debug_wait_timeout",
            "kv_append", "device_status", "build", "library", "MlaError"]
 
@@ -80,8 +82,11 @@ def library() -> ctypes.CDLL:
     lib.mla_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mla_debug_wait_timeout.argtypes = [vp]
     lib.mla_kv_append.argtypes = [vp, i64, vp, i64, vp, i64, f32, vp, i64, vp]
+    lib.mla_decode_step_static.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32,
+                                           vp, i64, vp, vp, vp, vp, vp, vp, vp]
     for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_decode_attend_planned", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
-                 "mla_device_status", "mla_choose_splits", "mla_kv_append", "mla_debug_wait_timeout"):
+                 "mla_device_status", "mla_choose_splits", "mla_kv_append", "mla_debug_wait_timeout",
+                 "mla_decode_step_static"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -442,3 +447,54 @@ def decode_step(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, *, h
     latent = torch.empty(o.shape[1:], dtype=torch.bfloat16, device=o.device)
     out = merge_value_gate(o, lse, w_uv, gate, lengths, qlen, latent=latent, lse_out=lse_m, stream=stream)
     return out, latent, lse_m
+
+
+def decode_step_static(q, kv, pages, indptr, scale, kv_scale, w_uv, gate, lengths, num_splits, split_tokens, *,
+                       heads=None, qlen=1, plan=None, out=None, latent=None, lse_out=None, stream=None):
+    """The whole step through ``mla_decode_step_static``: the split partials
+    live in the library's own 32 MiB device buffer, so the native call
+    allocates nothing (for callers that cannot allocate device memory while
+    they run; see the header).  Returns ``(out, latent, lse_out)``; the
+    outputs are allocated here with torch unless given.  Calls on one
+    device share the buffer: keep them ordered on one stream.  The first
+    call on a device looks up the buffer's address, so make it before any
+    stream capture.  Raises :class:`MlaError` (MLA_ERR_UNSUPPORTED) when the
+    partials, ``num_splits * S * heads * 1028`` bytes, do not fit."""
+    kv = _as_u8(kv)
+    heads = q.shape[1] if heads is None else heads
+    R = indptr.numel() - 1
+    S = R * qlen
+    _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == D_QK and q.stride(2) == 1
+          and q.stride(1) == D_QK, "q must be bf16 [S, H, 576] with contiguous [H, 576] heads")
+    _need(q.shape[0] == S and heads <= q.shape[1], "q shape does not match indptr / qlen / heads")
+    _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
+    _need(pages.dtype == torch.int32 and indptr.dtype == torch.int32 and pages.is_contiguous()
+          and indptr.is_contiguous(), "pages / indptr must be contiguous int32")
+    _need(w_uv.dtype == torch.bfloat16 and tuple(w_uv.shape) == (heads, D_V, D_LATENT) and w_uv.is_contiguous(),
+          "w_uv must be contiguous bf16 [heads, 128, 512]")
+    _need(gate.dtype == torch.bfloat16 and tuple(gate.shape) == (S, heads * D_V) and gate.is_contiguous(),
+          "gate must be contiguous bf16 [S, heads*128]")
+    _need(lengths.dtype == torch.int32 and lengths.numel() == R and lengths.is_contiguous(),
+          "lengths must be contiguous int32 [R]")
+    if plan is not None:
+        _need(plan.dtype == torch.int32 and plan.dim() == 1 and plan.is_contiguous(),
+              "plan must be a contiguous int32 device tensor")
+    _same_device(q.device, kv=kv, pages=pages, indptr=indptr, w_uv=w_uv, gate=gate, lengths=lengths, plan=plan,
+                 out=out, latent=latent, lse_out=lse_out)
+    if out is None:
+        out = torch.empty((S, heads * D_V), dtype=torch.bfloat16, device=q.device)
+    else:
+        _buffer(out, "out", torch.bfloat16, (S, heads * D_V))
+    if latent is None:
+        latent = torch.empty((S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    else:
+        _buffer(latent, "latent", torch.bfloat16, (S, heads, D_LATENT))
+    if lse_out is not None:
+        _buffer(lse_out, "lse_out", torch.float32, (S, heads))
+    st = library().mla_decode_step_static(
+        _ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr), R, qlen, heads,
+        float(scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(plan),
+        0 if plan is None else plan.numel(), _ptr(w_uv), _ptr(gate), _ptr(lengths), _ptr(out), _ptr(latent),
+        _ptr(lse_out), ctypes.c_void_p(_stream(stream, q.device.index)))
+    _check(st, "mla_decode_step_static")
+    return out, latent, lse_out

@@ -93,6 +93,11 @@ int device_sms() {
 
 }  // namespace
 
+namespace mla {
+// Error text for calls defined in other translation units (mla_last_error()).
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace mla
+
 extern "C" {
 
 mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
