@@ -408,7 +408,10 @@ struct TileIter {
         if (ok) {
             const int len = PAGED ? request_len(cur.indptr, ir, cur.num_pages, &base, cur.log2p, cur.last_page_len)
                                   : request_len(cur.indptr, ir, cur.num_pages, &base);
-            ok = (int64_t)s0 + c <= len;
+            // a range inside the request; a zero-token item only as the one
+            // split of an empty request (elsewhere it would write LSE -inf
+            // over partials other CTAs produce)
+            ok = (int64_t)s0 + c <= len && (c > 0 || (len == 0 && ik == 0 && inr == 1));
         }
         if (!ok) {
             flag(MLA_DEV_BAD_PLAN);

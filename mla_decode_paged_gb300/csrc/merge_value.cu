@@ -2,7 +2,8 @@
 //
 // What it computes: vLLM API page
 // vllm.models.kimi_k3.amd.specialized_decode.runtime.mla -- m1c_inputs
-// ("M1b merges the splits") and post (LSE combine, then W_UV and the gate);
+// (the split partials are merged by their LSE) and post (LSE combine, then
+// W_UV and the gate);
 // page vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value --
 // MlaValue / MlaGate (bf16 latent x W_UV with fp32 accumulation; value
 // rounded to bf16 times the fp32 sigmoid of the raw gate, rounded to bf16;
@@ -21,10 +22,12 @@
 // spreads over the SMs without a second wave (the host routes large
 // batches to the separate merge and value kernels, which read each partial
 // row once).
-// Launched with programmatic dependent launch: the W_UV copies and the gate
-// loads (inputs no earlier kernel writes) start while the attend grid is
-// still finishing; griddepcontrol.wait orders every read of the partials
-// and every global write after that grid's completion.
+// Launched with programmatic dependent launch: only the W_UV copies start
+// while the grid before it on the stream may still be running (W_UV is a
+// weight: nothing in the step writes it); griddepcontrol.wait orders every
+// other read (partials, gate, lengths) and every global write after that
+// grid's completion, so a kernel just before this one may produce any of
+// them.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -176,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1) merge_value_kernel(
         for (int i = lane; i < COLS; i += 32)
             bulk_g2s(sm.w[i], w_uv + ((long long)h * MLA_D_V + v0 + i) * MLA_D_LATENT, MLA_D_LATENT * 2, &sm.bar);
     }
+    // Everything below may come from the previous grid on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Gate words and row activity for the epilogue, in flight during the merge.
     uint32_t gw[2] = {0u, 0u};
     bool active[2] = {false, false};
@@ -188,8 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1) merge_value_kernel(
             if (active[hh]) gw[hh] = __ldg(reinterpret_cast<const uint32_t *>(gate + rowoff + 8 * warp + 2 * qd));
         }
     }
-    // The partials come from the previous grid on the stream.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     // One latent row per warp into smem.
     {
         const long long nrow = (long long)S * H;
@@ -204,7 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1) merge_value_kernel(
     }
     __syncthreads();
     if (warp >= MW) return;
-    if (!mbar_wait(&sm.bar, 0)) return;
+    if (!mbar_wait(&sm.bar, 0)) {
+        // Flagged; before the CTA may exit (and its shared memory be reused)
+        // give the W_UV copies one more bounded wait to land.
+        mbar_wait(&sm.bar, 0);
+        return;
+    }
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8

@@ -73,7 +73,12 @@ __global__ void __launch_bounds__(kThreads) value_gate_kernel(
         for (int n = 0; n < 4; ++n)
             gw[hh][n] = active[hh] ? __ldg(reinterpret_cast<const uint32_t *>(gate + rowoff + 8 * n + 2 * qd)) : 0u;
     }
-    if (!mbar_wait(&sm.bar, 0)) return;
+    if (!mbar_wait(&sm.bar, 0)) {
+        // Flagged; before the CTA may exit (and its shared memory be reused)
+        // give the bulk copies one more bounded wait to land.
+        mbar_wait(&sm.bar, 0);
+        return;
+    }
 
     float acc[4][4];
 #pragma unroll

@@ -10,6 +10,7 @@ import torch
 import mla_decode_paged_gb300 as mla
 from mla_decode_paged_gb300 import workloads as W
 from oracle import mla_oracle as O
+from tests import _full as F
 from tests import _plan
 from tests._bits import bf16_bits, i32, oracle_args, u8
 from tests.parity import assert_bf16_close, assert_lse_close, to_f64
@@ -113,28 +114,17 @@ def test_planned_fp8_query_matches_oracle():
 
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_planned_full_size_workloads(idx):
-    """The launch configuration the benchmark times: merged output checked
-    against the oracle on sampled requests and against the round-robin
-    launch everywhere."""
+def test_planned_full_size_workloads(idx, capsys):
+    """The launch configuration the benchmark times (the host work plan cuts
+    requests at arbitrary tile boundaries across CTAs): the merged LSE and
+    latent of every request against the oracle."""
     inp = W.make_inputs(idx, DEV)
     ns, st = mla.choose_splits(inp.spec.requests, inp.qlen, inp.heads, lengths=inp.lengths.cpu())
     plan, used = mla.plan_units(inp.lengths.cpu(), inp.qlen, inp.heads, ns)
     latent, lse_m = mla.merge(*_attend(inp, used, plan))
-    rr_lat, rr_lse = mla.merge(*_attend(inp, ns, st=st))
     torch.cuda.synchronize()
-    lens = i32(inp.lengths)
-    rng = np.random.default_rng(idx)
-    reqs = sorted(set([int(lens.argmax())] + [int(x) for x in rng.choice(len(lens), 2, replace=False)]))
-    a = dict(q_bits=bf16_bits(inp.q), kv_codes=u8(inp.kv), pages=i32(inp.pages), indptr=i32(inp.indptr),
-             scale=inp.scale, kv_scale=inp.kv_scale, heads=inp.heads, qlen=inp.qlen)
-    rlat, rlse = O.attend(**a, requests=reqs)
-    rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
-    assert_lse_close(lse_m[rows], rlse[rows], "planned lse (sampled)")
-    assert_bf16_close(latent[rows], rlat[rows], "planned latent (sampled)")
-    # every row: the planned and round-robin launches agree to rounding
-    assert_lse_close(lse_m, to_f64(rr_lse), "planned vs round-robin lse")
-    assert_bf16_close(latent, to_f64(rr_lat), "planned vs round-robin latent")
+    ref = F.reference(("plain", idx), inp)
+    F.check_every_row("%s with the work plan" % inp.spec.name, ref, latent, lse_m, capsys=capsys)
     assert mla.device_status() == 0
 
 
@@ -181,6 +171,7 @@ def test_plan_offsets_outside_the_buffer_are_flagged():
     ("k", 0 | (1 << 9) | (1 << 18)),   # row group past the groups (1)
     ("start", -128),
     ("count", 1 << 20),  # past the request's tokens
+    ("count", 0),        # no tokens for a request that has some (only an empty request's one split may)
 ])
 def test_plan_items_outside_the_launch_are_flagged(field, value):
     inp, plan = _small()
