@@ -11,8 +11,8 @@
  *
  * Sources (vLLM API pages):
  *   - vllm.models.kimi_k3.amd.specialized_decode.runtime.mla: attend,
- *     m1c_inputs, post (the decode split, the flat token rows, the padded
- *     query, the partials and their merge);
+ *     m1c_inputs, post (the decode split, the cache as one 576-byte row per
+ *     token, the padded query, the partials and their merge);
  *   - vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.value:
  *     MlaValue, MlaGate, value_bmm (W_UV and the gate).
  *
@@ -64,8 +64,8 @@ typedef int mla_status;
  * mla_decode_attend -- split-KV attention of one decode step.
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
- * m1c_inputs (inputs q [S, 12, 576] bf16, kv = the flat token rows, pages =
- * paged_kv_indices, indptr = paged_kv_indptr, scale, kv_scale; outputs the
+ * m1c_inputs (inputs q [S, 12, 576] bf16, kv = one 576-byte row per token,
+ * pages = paged_kv_indices, indptr = paged_kv_indptr, scale, kv_scale; outputs the
  * partials o [splits, S, 12, 512] bf16 and LSE [splits, S, 12] f32) and
  * attend (multi-query attention over the latent cache; a query whose row
  * stride spans padded heads).
@@ -122,12 +122,11 @@ mla_status mla_decode_attend(const void *q, int64_t q_row_stride, const void *kv
  *
  * MLA_ATTEND_Q_FP8: q holds e4m3 codes, one byte per element (the pages'
  * decode-context-parallel input q8, whose _q_scale multiplies every score:
- * pass scale * q_scale as scale); q_row_stride counts bytes and must be a
+ * here pass scale * q_scale as scale, or give q_scale to
+ * mla_decode_attend_planned); q_row_stride counts bytes and must be a
  * multiple of 16.  The score is scale * <e4m3(q), K>.
  *
  * Arguments as mla_decode_attend.  Unknown flag bits: MLA_ERR_INVALID.
- * MLA_ATTEND_CAUSAL or MLA_ATTEND_Q_FP8 with the warp-MMA kernel
- * (environment MLA_ATTEND_KERNEL=mma): MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void *kv,
                                 int64_t pool_rows, const int32_t *pages, int64_t num_pages,
@@ -138,7 +137,7 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
 /*
  * mla_decode_attend_paged -- mla_decode_attend_ex over a block-table cache.
  *
- * The pages address "the flat token rows" one row per entry (m1c_inputs:
+ * The pages address the cache one 576-byte row per page index (m1c_inputs:
  * page size 1).  vLLM's paged layout groups page_size rows per block: here
  * pages holds block indices, indptr[r+1] - indptr[r] counts request r's
  * blocks, the last block holds last_page_len[r] rows, and token j of
@@ -152,7 +151,6 @@ mla_status mla_decode_attend_ex(const void *q, int64_t q_row_stride, const void 
  *   last_page_len  int32 [num_requests], device, each in 1..page_size for a
  *                  request with blocks (else MLA_DEV_BAD_INDPTR, request empty).
  * A block index whose rows fall outside the pool sets MLA_DEV_BAD_PAGE.
- * page_size > 1 with the warp-MMA kernel: MLA_ERR_UNSUPPORTED.
  */
 mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const void *kv,
                                    int64_t pool_rows, const int32_t *pages, int64_t num_pages,
@@ -216,16 +214,20 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
  * and the merged result is the same attention up to rounding.  A plan for
  * another grid, offsets outside the buffer, or an item outside the launch
  * (r >= num_requests, k >= n_r, n_r > num_splits, group >= the row groups,
- * a range past the request's tokens) sets MLA_DEV_BAD_PLAN and ends that
- * CTA's list, leaving its remaining splits unwritten.  A plan with plan_len
- * < 3 or > 2^31 - 1, or not 4-byte aligned: MLA_ERR_INVALID; a plan with the
- * warp-MMA kernel: MLA_ERR_UNSUPPORTED.
+ * a range past the request's tokens, a zero-token item for a request that
+ * has tokens) sets MLA_DEV_BAD_PLAN and ends that CTA's list, leaving its
+ * remaining splits unwritten.  A plan with plan_len < 3 or > 2^31 - 1, or
+ * not 4-byte aligned: MLA_ERR_INVALID.
+ *
+ * q_scale multiplies every score (the pages' _q_scale of an fp8 query,
+ * MLA_ATTEND_Q_FP8; 1 for a bf16 query): the score is
+ * scale * q_scale * <q, K>.  It must be finite.
  */
 mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv,
                                      int64_t pool_rows, const int32_t *pages, int64_t num_pages,
                                      const int32_t *indptr, const int32_t *last_page_len,
                                      int page_size, int num_requests, int qlen, int heads,
-                                     float scale, float kv_scale, int num_splits,
+                                     float scale, float kv_scale, float q_scale, int num_splits,
                                      int split_tokens, void *o, float *lse, unsigned int flags,
                                      const int32_t *plan, int64_t plan_len, void *stream);
 
@@ -233,7 +235,7 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
  * mla_merge_splits -- LSE merge of split partials into the latent.
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
- * m1c_inputs ("M1b merges the splits") and post (the same LSE combine
+ * m1c_inputs (the split partials are merged by their LSE) and post (the same LSE combine
  * across decode-context-parallel ranks).  For every row t < rows, head h:
  *   LSE = ln sum_k exp(lse[k, t, h])   over splits with lse > -inf
  *   latent[t, h, :] = sum_k exp(lse[k, t, h] - LSE) * o[k, t, h, :]
@@ -285,6 +287,11 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
  *   w_uv, gate, lengths  as mla_value_gate;  out bf16 [S, heads*128] (written)
  *   latent               bf16 [S, heads, 512] (written: the merged latent)
  *   lse_out              f32 [S, heads] (written; may be NULL)
+ *
+ * The one-launch route starts reading w_uv before the kernel enqueued just
+ * before it on the stream has finished (programmatic dependent launch; every
+ * other input is read after that kernel completes): w_uv must not be
+ * written by that kernel.
  */
 mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits, const void *w_uv,
                                 const void *gate, const int32_t *lengths, int num_requests, int qlen,
@@ -296,7 +303,7 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla, pre
  * (do_kv_cache_update: each new token's kv_c (512 latent values) and k_pe
  * (64 rope values) are stored, scaled by 1/_k_scale and converted to fp8,
- * at the token's slot of the flat token rows that mla_decode_attend reads).
+ * at the token's slot: the row of the cache that mla_decode_attend reads).
  * For token i with slots[i] >= 0 and every d < 576:
  *   kv[slots[i], d] = e4m3(x / k_scale),  x = kv_c[i, d] (d < 512) or k_pe[i, d - 512]
  * with the quotient in float32 (IEEE division) and e4m3 round-to-nearest-
@@ -341,6 +348,19 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
 mla_status mla_debug_gather(const void *kv, int64_t pool_rows, const int32_t *pages,
                             int64_t num_pages, const int32_t *indptr, int num_requests,
                             int64_t total_rows, void *out, void *stream);
+
+/*
+ * mla_debug_attend_mma -- a second, independently written attend kernel,
+ * kept as a cross-check for the tests (no counterpart on the pages: it
+ * computes what mla_decode_attend computes, with warp-level mma.sync f16
+ * MMAs on e4m3 -> f16 converted rows instead of tcgen05 tensor memory).
+ * Arguments, outputs and split rule as mla_decode_attend (page size 1,
+ * bf16 query, no mask, no work plan).  Not used by any other call.
+ */
+mla_status mla_debug_attend_mma(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                const int32_t *pages, int64_t num_pages, const int32_t *indptr,
+                                int num_requests, int qlen, int heads, float scale, float kv_scale,
+                                int num_splits, int split_tokens, void *o, float *lse, void *stream);
 
 /*
  * mla_debug_wait_timeout -- test hook for the device-side failure path (no

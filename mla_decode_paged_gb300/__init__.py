@@ -32,7 +32,7 @@ STATIC_SCRATCH_BYTES = 32 << 20   # MLA_STATIC_SCRATCH_BYTES: the partials buffe
 
 __all__ = ["Prepared", "attend", "merge", "value_gate", "merge_value_gate", "decode_step", "decode_step_static",
            "STATIC_SCRATCH_BYTES", "choose_splits", "plan_units", "debug_gather",
-           "debug_wait_timeout",
+           "debug_wait_timeout", "debug_attend_mma",
            "kv_append", "device_status", "build", "library", "MlaError"]
 
 
@@ -71,7 +71,9 @@ def library() -> ctypes.CDLL:
     lib.mla_decode_attend_paged.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
                                             i32, i32, vp, vp, ctypes.c_uint, vp]
     lib.mla_decode_attend_planned.argtypes = [vp, i64, vp, i64, vp, i64, vp, vp, i32, i32, i32, i32, f32, f32,
-                                              i32, i32, vp, vp, ctypes.c_uint, vp, i64, vp]
+                                              f32, i32, i32, vp, vp, ctypes.c_uint, vp, i64, vp]
+    lib.mla_debug_attend_mma.argtypes = [vp, i64, vp, i64, vp, i64, vp, i32, i32, i32, f32, f32, i32, i32, vp, vp,
+                                         vp]
     lib.mla_plan_units.argtypes = [i32, i32, i32, vp, i32, i32, vp, i64, ctypes.POINTER(ctypes.c_int)]
     lib.mla_plan_units.restype = i64
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
@@ -86,7 +88,7 @@ def library() -> ctypes.CDLL:
                                            vp, i64, vp, vp, vp, vp, vp, vp, vp]
     for name in ("mla_decode_attend", "mla_decode_attend_ex", "mla_decode_attend_paged", "mla_decode_attend_planned", "mla_merge_splits", "mla_value_gate", "mla_merge_value_gate", "mla_debug_gather",
                  "mla_device_status", "mla_choose_splits", "mla_kv_append", "mla_debug_wait_timeout",
-                 "mla_decode_step_static"):
+                 "mla_decode_step_static", "mla_debug_attend_mma"):
         getattr(lib, name).restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -231,7 +233,7 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
               "plan must be a contiguous int32 device tensor")
     args = (_ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(), _ptr(indptr),
             _ptr(last_page_len) if page_size > 1 else None, int(page_size), R, qlen,
-            heads, float(scale) * float(q_scale), float(kv_scale), int(num_splits), int(split_tokens), _ptr(o),
+            heads, float(scale), float(kv_scale), float(q_scale), int(num_splits), int(split_tokens), _ptr(o),
             _ptr(lse), (ATTEND_CAUSAL if causal else 0) | (ATTEND_Q_FP8 if q8 else 0), _ptr(plan),
             0 if plan is None else plan.numel())
     lib = library()
@@ -242,6 +244,38 @@ def attend(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, h
                         (q, kv, pages, indptr, last_page_len, plan))
     st = lib.mla_decode_attend_planned(*args, ctypes.c_void_p(_stream(stream, q.device.index)))
     _check(st, "mla_decode_attend")
+    return o, lse
+
+
+def debug_attend_mma(q, kv, pages, indptr, scale, kv_scale, num_splits, split_tokens, *, heads=None, qlen=1,
+                     o=None, lse=None, stream=None):
+    """The same partials as :func:`attend` (page size 1, bf16 query, no
+    options) from the library's second attend kernel, the warp-MMA one that
+    the tests run as a cross-check (``mla_debug_attend_mma``)."""
+    kv = _as_u8(kv)
+    heads = q.shape[1] if heads is None else heads
+    R = indptr.numel() - 1
+    S = R * qlen
+    _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == D_QK and q.stride(2) == 1
+          and q.stride(1) == D_QK, "q must be bf16 [S, H, 576] with contiguous [H, 576] heads")
+    _need(q.shape[0] == S and heads <= q.shape[1], "q shape does not match indptr / qlen / heads")
+    _need(kv.dim() == 2 and kv.shape[1] == D_QK and kv.is_contiguous(), "kv must be contiguous [pool, 576]")
+    _need(pages.dtype == torch.int32 and indptr.dtype == torch.int32 and pages.is_contiguous()
+          and indptr.is_contiguous(), "pages / indptr must be contiguous int32")
+    _same_device(q.device, kv=kv, pages=pages, indptr=indptr, o=o, lse=lse)
+    if o is None:
+        o = torch.empty((num_splits, S, heads, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    else:
+        _buffer(o, "o", torch.bfloat16, (num_splits, S, heads, D_LATENT))
+    if lse is None:
+        lse = torch.empty((num_splits, S, heads), dtype=torch.float32, device=q.device)
+    else:
+        _buffer(lse, "lse", torch.float32, (num_splits, S, heads))
+    st = library().mla_debug_attend_mma(_ptr(q), q.stride(0), _ptr(kv), kv.shape[0], _ptr(pages), pages.numel(),
+                                        _ptr(indptr), R, qlen, heads, float(scale), float(kv_scale), int(num_splits),
+                                        int(split_tokens), _ptr(o), _ptr(lse),
+                                        ctypes.c_void_p(_stream(stream, q.device.index)))
+    _check(st, "mla_debug_attend_mma")
     return o, lse
 
 

@@ -65,14 +65,6 @@ mla_status cuda_fail(cudaError_t e, const char *where) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Which attend kernel runs: the tensor-memory (tcgen05) kernel unless the
-// environment variable MLA_ATTEND_KERNEL is "mma" (the warp-MMA kernel),
-// for A/B measurements and tests.
-bool use_warp_mma() {
-    const char *v = std::getenv("MLA_ATTEND_KERNEL");
-    return v && std::string(v) == "mma";
-}
-
 // The current device's SM count, or 0 when there is no usable device (the
 // callers then fail with MLA_ERR_CUDA rather than size a grid for a guess).
 int device_sms() {
@@ -124,16 +116,16 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
                                    int heads, float scale, float kv_scale, int num_splits, int split_tokens,
                                    void *o, float *lse, unsigned int flags, void *stream) {
     return mla_decode_attend_planned(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, last_page_len,
-                                     page_size, num_requests, qlen, heads, scale, kv_scale, num_splits,
+                                     page_size, num_requests, qlen, heads, scale, kv_scale, 1.0f, num_splits,
                                      split_tokens, o, lse, flags, nullptr, 0, stream);
 }
 
 mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
                                      const int32_t *pages, int64_t num_pages, const int32_t *indptr,
                                      const int32_t *last_page_len, int page_size, int num_requests, int qlen,
-                                     int heads, float scale, float kv_scale, int num_splits, int split_tokens,
-                                     void *o, float *lse, unsigned int flags, const int32_t *plan,
-                                     int64_t plan_len, void *stream) {
+                                     int heads, float scale, float kv_scale, float q_scale, int num_splits,
+                                     int split_tokens, void *o, float *lse, unsigned int flags,
+                                     const int32_t *plan, int64_t plan_len, void *stream) {
     if (flags & ~(MLA_ATTEND_CAUSAL | MLA_ATTEND_Q_FP8)) return fail(MLA_ERR_INVALID, "unknown flag bits");
     if (plan && (plan_len < 3 || plan_len > INT32_MAX || !aligned(plan, 4)))
         return fail(MLA_ERR_INVALID, "plan too short, too long or misaligned");
@@ -154,7 +146,8 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
         return fail(MLA_ERR_INVALID, q8 ? "q_row_stride must be >= heads*576 and a multiple of 16 (fp8 q)"
                                         : "q_row_stride must be >= heads*576 and a multiple of 8");
     if (pool_rows < 0 || num_pages < 0) return fail(MLA_ERR_INVALID, "negative pool_rows / num_pages");
-    if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return fail(MLA_ERR_INVALID, "non-finite scale");
+    if (!std::isfinite(scale) || !std::isfinite(kv_scale) || !std::isfinite(q_scale))
+        return fail(MLA_ERR_INVALID, "non-finite scale");
     if (num_requests == 0) return MLA_OK;
     if (!q || !kv || !indptr || !o || !lse || (num_pages > 0 && !pages))
         return fail(MLA_ERR_INVALID, "null pointer");
@@ -165,22 +158,45 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
     if (pool_rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "pool_rows above 2^31 - 1");
     if (page_size > 1 && (!last_page_len || !aligned(last_page_len, 4)))
         return fail(MLA_ERR_INVALID, "page_size > 1 needs last_page_len (int32, 4-byte aligned)");
-    if (causal && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "causal mask with the warp-MMA kernel");
-    if (page_size > 1 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "page_size > 1 with the warp-MMA kernel");
-    if (q8 && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "fp8 query with the warp-MMA kernel");
-    if (plan && use_warp_mma()) return fail(MLA_ERR_UNSUPPORTED, "work plan with the warp-MMA kernel");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int sms = device_sms();
     if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
-    cudaError_t e = use_warp_mma()
-                        ? mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
-                                                 num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                 split_tokens, o, lse, sms, st)
-                        : mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr,
-                                                num_requests, qlen, heads, scale, kv_scale, num_splits,
-                                                split_tokens, o, lse, causal, log2p, last_page_len, q8, plan,
-                                                plan_len, sms, st);
+    // The fp8 query's scale multiplies every score: folded into the softmax scale.
+    cudaError_t e = mla::attend_tc_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, num_requests,
+                                          qlen, heads, scale * q_scale, kv_scale, num_splits, split_tokens, o, lse,
+                                          causal, log2p, last_page_len, q8, plan, plan_len, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+    return MLA_OK;
+}
+
+mla_status mla_debug_attend_mma(const void *q, int64_t q_row_stride, const void *kv, int64_t pool_rows,
+                                const int32_t *pages, int64_t num_pages, const int32_t *indptr, int num_requests,
+                                int qlen, int heads, float scale, float kv_scale, int num_splits, int split_tokens,
+                                void *o, float *lse, void *stream) {
+    // The argument rules of mla_decode_attend (page size 1, bf16 query,
+    // no options), then the warp-MMA kernel.
+    if (num_requests < 0) return fail(MLA_ERR_INVALID, "num_requests < 0");
+    if (qlen < 1 || qlen > MLA_MAX_QLEN) return fail(MLA_ERR_INVALID, "qlen outside 1..16");
+    if (heads < 1 || heads > MLA_MAX_HEADS) return fail(MLA_ERR_INVALID, "heads outside 1..128");
+    if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return fail(MLA_ERR_INVALID, "num_splits outside 1..256");
+    if (split_tokens < 1) return fail(MLA_ERR_INVALID, "split_tokens < 1");
+    if (q_row_stride < (int64_t)heads * MLA_D_QK || q_row_stride % 8 != 0)
+        return fail(MLA_ERR_INVALID, "q_row_stride must be >= heads*576 and a multiple of 8");
+    if (pool_rows < 0 || num_pages < 0) return fail(MLA_ERR_INVALID, "negative pool_rows / num_pages");
+    if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return fail(MLA_ERR_INVALID, "non-finite scale");
+    if (num_requests == 0) return MLA_OK;
+    if (!q || !kv || !indptr || !o || !lse || (num_pages > 0 && !pages)) return fail(MLA_ERR_INVALID, "null pointer");
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(indptr, 4) ||
+        !aligned(pages, 4))
+        return fail(MLA_ERR_INVALID, "misaligned pointer (q, kv, o need 16 bytes)");
+    if (pool_rows == 0) return fail(MLA_ERR_INVALID, "empty KV pool");
+    if (pool_rows > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "pool_rows above 2^31 - 1");
+    const int sms = device_sms();
+    if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
+    cudaError_t e = mla::attend_mma_launch(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, num_requests,
+                                           qlen, heads, scale, kv_scale, num_splits, split_tokens, o, lse, sms,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "warp-MMA attend launch");
     return MLA_OK;
 }
 
@@ -274,7 +290,8 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
     }
     if (total_len <= 0) total_len = (int64_t)num_requests * max_len;
     const int rows = qlen * heads;
-    const int groups = use_warp_mma() ? (rows + 63) / 64 : (rows + 47) / 48;
+    int groups = 1, nq = 16;
+    mla::attend_tc_shape(rows, &groups, &nq);
     const double bw_sm = 6.5e12 / sm_count;   // bytes/s per SM at the HBM roofline
     const double t_tok = MLA_D_QK / bw_sm;     // seconds per KV row on one SM
     const double t_unit = 1.5e-6;              // per-unit start-up (query load, epilogue)

@@ -128,7 +128,7 @@ struct Misc {
     const int32_t *indptr;                                                                          \
     int R, qlen, heads, num_splits, split_tokens, row_groups;                                       \
     PAD                                                                                             \
-    int log2p;                    /* blocks of 2^log2p rows (0: flat token rows) */                 \
+    int log2p;                    /* blocks of 2^log2p rows (0: one row per page) */                 \
     int q8;                       /* q holds e4m3 codes (row stride in bytes) */                    \
     const int32_t *plan;          /* work plan (null: units dealt round robin) */                   \
     int plan_len;                 /* its length in int32 (the host caps it at INT32_MAX) */         \

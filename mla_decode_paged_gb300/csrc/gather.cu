@@ -3,7 +3,8 @@
 // into shared memory that the attend kernels use, so that page indexing can
 // be checked byte for byte against a host gather.  Paged rows: vLLM API
 // page vllm.models.kimi_k3.amd.specialized_decode.runtime.mla, m1c_inputs
-// (kv = the flat token rows, pages = paged_kv_indices, indptr).
+// (kv viewed as one 576-byte row per token, pages = paged_kv_indices,
+// indptr).
 #include <cuda_runtime.h>
 
 #include "common.cuh"

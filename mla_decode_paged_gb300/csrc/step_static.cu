@@ -101,8 +101,8 @@ mla_status mla_decode_step_static(const void *q, int64_t q_row_stride, const voi
     void *o = scratch;
     float *lse = reinterpret_cast<float *>(scratch + lse_off);
     mla_status s = mla_decode_attend_planned(q, q_row_stride, kv, pool_rows, pages, num_pages, indptr, nullptr, 1,
-                                             num_requests, qlen, heads, scale, kv_scale, num_splits, split_tokens,
-                                             o, lse, 0u, plan, plan_len, stream);
+                                             num_requests, qlen, heads, scale, kv_scale, 1.0f, num_splits,
+                                             split_tokens, o, lse, 0u, plan, plan_len, stream);
     if (s != MLA_OK) return s;
     return mla_merge_value_gate(o, lse, num_splits, w_uv, gate, lengths, num_requests, qlen, heads, out, latent,
                                 lse_out, stream);

@@ -101,10 +101,40 @@ def test_attend_ex_rejects_unknown_flags_and_checks_like_attend(lib):
     assert _attend_ex(lib, mla.ATTEND_CAUSAL, R=0) == mla.MLA_OK
 
 
-def test_causal_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
+@pytest.mark.parametrize("kw,msg", [
+    (dict(R=-1), b"num_requests"),
+    (dict(qlen=17), b"qlen"),
+    (dict(heads=129), b"heads"),
+    (dict(num_splits=0), b"num_splits"),
+    (dict(split_tokens=0), b"split_tokens"),
+    (dict(q_row_stride=12 * 576 + 4), b"q_row_stride"),
+    (dict(o=NULL), b"null"),
+    (dict(kv=ctypes.c_void_p((1 << 20) + 8)), b"misaligned"),
+    (dict(pool_rows=0), b"empty KV pool"),
+    (dict(kv_scale=float("inf")), b"non-finite"),
+])
+def test_warp_mma_cross_check_checks_like_attend(lib, kw, msg):
+    """The tests' second attend kernel (mla_debug_attend_mma) refuses the
+    arguments mla_decode_attend refuses, before any launch."""
+    a = dict(q=P16, q_row_stride=12 * 576, kv=P16, pool_rows=100, pages=P16, num_pages=10, indptr=P16,
+             R=2, qlen=1, heads=12, scale=0.1, kv_scale=1.0, num_splits=4, split_tokens=16, o=P16, lse=P16,
+             stream=NULL)
+    a.update(kw)
+    st = lib.mla_debug_attend_mma(a["q"], a["q_row_stride"], a["kv"], a["pool_rows"], a["pages"], a["num_pages"],
+                                  a["indptr"], a["R"], a["qlen"], a["heads"], a["scale"], a["kv_scale"],
+                                  a["num_splits"], a["split_tokens"], a["o"], a["lse"], a["stream"])
+    assert st == (mla.MLA_ERR_UNSUPPORTED if kw.get("pool_rows", 1) > 2**31 else mla.MLA_ERR_INVALID)
+    assert msg in lib.mla_last_error()
+
+
+def test_no_environment_switch_changes_the_attend_kernel(lib, monkeypatch):
+    """The product calls always run the tcgen05 kernel: the warp-MMA kernel is
+    reachable only through its own test entry point, so options it lacks are
+    never refused because of the environment."""
     monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
-    assert _attend_ex(lib, mla.ATTEND_CAUSAL) == mla.MLA_ERR_UNSUPPORTED
-    assert b"causal" in lib.mla_last_error()
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL, R=0) == mla.MLA_OK
+    assert _attend_ex(lib, mla.ATTEND_CAUSAL, qlen=0) == mla.MLA_ERR_INVALID
+    assert b"qlen" in lib.mla_last_error()
 
 
 def test_merge_and_value_gate_reject_bad_arguments(lib):
@@ -207,17 +237,8 @@ def test_attend_paged_needs_last_page_len(lib):
     assert _attend_paged(lib, 16, last=ctypes.c_void_p((1 << 20) + 2)) == mla.MLA_ERR_INVALID
 
 
-def test_attend_paged_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
-    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
-    assert _attend_paged(lib, 16) == mla.MLA_ERR_UNSUPPORTED
-    assert b"page_size" in lib.mla_last_error()
-
-
-def test_fp8_query_flag_checks(lib, monkeypatch):
+def test_fp8_query_flag_checks(lib):
     # fp8 rows: the stride counts bytes and must be a multiple of 16
     assert _attend_ex(lib, mla.ATTEND_Q_FP8, q_row_stride=12 * 576 + 8) == mla.MLA_ERR_INVALID
     assert b"multiple of 16" in lib.mla_last_error()
     assert _attend_ex(lib, mla.ATTEND_Q_FP8 | 4) == mla.MLA_ERR_INVALID
-    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
-    assert _attend_ex(lib, mla.ATTEND_Q_FP8) == mla.MLA_ERR_UNSUPPORTED
-    assert b"fp8 query" in lib.mla_last_error()

@@ -127,9 +127,9 @@ def test_plan_size_query_and_errors(lib):
     assert lib.mla_plan_units(2, 1, 96, lp, 4, 1, None, 0, None) == mla.MLA_ERR_UNSUPPORTED
 
 
-def _attend_planned(lib, plan, plan_len, page_size=1, last=NULL):
+def _attend_planned(lib, plan, plan_len, page_size=1, last=NULL, q_scale=1.0):
     return lib.mla_decode_attend_planned(P16, 12 * 576, P16, 128, P16, 10, P16, last, page_size, 2, 1, 12, 0.1, 1.0,
-                                         4, 16, P16, P16, 0, plan, plan_len, NULL)
+                                         q_scale, 4, 16, P16, P16, 0, plan, plan_len, NULL)
 
 
 def test_planned_attend_rejects_short_or_misaligned_plans(lib):
@@ -139,7 +139,6 @@ def test_planned_attend_rejects_short_or_misaligned_plans(lib):
     assert b"plan" in lib.mla_last_error()
 
 
-def test_planned_attend_with_warp_mma_kernel_is_unsupported(lib, monkeypatch):
-    monkeypatch.setenv("MLA_ATTEND_KERNEL", "mma")
-    assert _attend_planned(lib, P16, 20) == mla.MLA_ERR_UNSUPPORTED
-    assert b"work plan" in lib.mla_last_error()
+def test_planned_attend_rejects_a_non_finite_q_scale(lib):
+    assert _attend_planned(lib, P16, 20, q_scale=float("nan")) == mla.MLA_ERR_INVALID
+    assert b"non-finite" in lib.mla_last_error()
