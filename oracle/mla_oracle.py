@@ -86,10 +86,10 @@ def sigmoid(x) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def request_rows(pages, indptr, r: int, page_size: int = 1, last_page_len=None) -> np.ndarray:
-    """Row indices of request r's tokens in the flat token rows, in order.
+    """Row indices of request r's tokens in the KV pool, in order.
 
-    Page size 1 (``m1c_inputs``: "the flat token rows"): ``pages[indptr[r]:
-    indptr[r+1]]``.  Page size P > 1 (vLLM block tables): ``pages`` holds
+    Page size 1 (``m1c_inputs`` views the cache as one 576-wide row per
+    token): ``pages[indptr[r]:indptr[r+1]]``.  Page size P > 1 (vLLM block tables): ``pages`` holds
     block indices and ``indptr`` counts blocks; block b covers rows
     [b*P, (b+1)*P); the request's last block holds ``last_page_len[r]``
     tokens, so L_r = (blocks - 1) * P + last_page_len[r] and token j is row
@@ -107,8 +107,8 @@ def request_rows(pages, indptr, r: int, page_size: int = 1, last_page_len=None) 
 
 
 def gather_rows(kv_codes, pages, indptr, r: int, page_size: int = 1, last_page_len=None) -> np.ndarray:
-    """Request r's KV rows, as raw fp8 codes [L_r, 576]: the flat token rows
-    ``kv.view(-1, 576)`` addressed through :func:`request_rows`
+    """Request r's KV rows, as raw fp8 codes [L_r, 576]: the cache viewed as
+    ``kv.view(-1, 576)``, one row per token, addressed through :func:`request_rows`
     (``m1c_inputs``: ``kv``, ``pages``, ``indptr``)."""
     kv_codes = np.asarray(kv_codes, dtype=np.uint8)
     return kv_codes[request_rows(pages, indptr, r, page_size, last_page_len)]
@@ -160,7 +160,13 @@ def attend_rows(q_rows, K, scale: float, visible=None):
         denom = e.sum()
         p[i, :v] = e / denom
         lse[i] = m + np.log(denom)
-        latent[i] = p[i, :v] @ K[:v, :D_LATENT]
+    # latent = p @ V, one matrix product per group of rows that see the same
+    # number of tokens (every row at once without a mask)
+    for v in np.unique(vis):
+        if v == 0:
+            continue
+        sel = vis == v
+        latent[sel] = p[sel, :v] @ K[:v, :D_LATENT]
     return latent, lse, p
 
 
@@ -172,10 +178,18 @@ def causal_visible(L: int, qlen: int, heads: int) -> np.ndarray:
     return np.clip(int(L) - qlen + tq + 1, 0, int(L))
 
 
+_E4M3_TABLE = None
+
+
 def dequant(codes, kv_scale: float) -> np.ndarray:
     """``e4m3fn(code) * kv_scale`` in float64 (the cache holds x / k_scale as
-    fp8; ``m1c_inputs`` passes ``kv_scale=attn._k_scale_float``)."""
-    return e4m3fn_to_f64(codes) * float(kv_scale)
+    fp8; ``m1c_inputs`` passes ``kv_scale=attn._k_scale_float``).  The codes
+    are looked up in the 256 values :func:`e4m3fn_to_f64` gives (the same
+    numbers, without its full-size temporaries)."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        _E4M3_TABLE = e4m3fn_to_f64(np.arange(256, dtype=np.uint8))
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)] * float(kv_scale)
 
 
 def query_rows(q, t0: int, t1: int, heads: int, q_fp8: bool = False) -> np.ndarray:
@@ -396,7 +410,7 @@ def kv_append(kv_codes, kv_c_bits, k_pe_bits, slots, k_scale: float) -> np.ndarr
     ``vllm.models.kimi_k3.amd.specialized_decode.runtime.mla``, ``pre``:
     ``do_kv_cache_update`` stores the 512-wide ``kv_c`` and the 64-wide
     ``k_pe`` of each token, divided by ``k_scale`` and converted to fp8, at
-    the token's slot of the flat token rows).
+    the token's slot, the row of the pool that attend later reads).
 
     ``kv_codes``: uint8 [pool, 576] (not modified; a copy is returned);
     ``kv_c_bits``: bf16 bits [T, 512]; ``k_pe_bits``: bf16 bits [T, 64];
