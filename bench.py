@@ -4,18 +4,22 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints ONE JSON line (rank 0).  A step is one pass of the whole path over
-one batch of the workload (default: 64 single-token requests, 12 heads,
-context lengths uniform in [1024, 8192], fp8 KV), inputs resident in HBM.
-L2 is flushed (a 256 MB write) before every timed step; only the step is
-inside the CUDA events.  ``value`` is query rows (tokens) per second over
-all ranks, the step's launches replayed from one captured CUDA graph;
-``kernels_us`` and the roofline come from a second, eager pass with an
-event around each launch.  ``e2e`` repeats the step through the public API with the step's
-inputs copied from pinned host memory and its output read back, inside
-the timed region.  ``roofline`` is the attend kernel's algorithmic HBM bytes
-per launch over its event-timed duration, against the measured copy
-bandwidth.  ``cpu_baseline`` times the plain C fp64 oracle on the host
-cores over a bounded sample of the same workload.
+one batch of the workload, inputs resident in HBM.  The default workload is
+the largest: 256 requests x 8 query rows (2,048 rows), 12 heads, context
+lengths log-uniform in [128, 131072] with 8 empty requests, fp8 KV (about
+2.7 GB of KV rows per step).  L2 is flushed (a 256 MB write) before every
+timed step; only the step is inside the CUDA events.  ``value`` is query rows
+(tokens) per second over all ranks, the step's launches replayed from one
+captured CUDA graph; ``kernels_us`` and the roofline come from a second,
+eager pass with an event around each launch.  ``e2e`` repeats the step
+through the public API with the step's inputs copied from pinned host memory
+and its output read back, inside the timed region.  ``roofline`` is the
+attend kernel's algorithmic HBM bytes per launch over its event-timed
+duration, against the measured copy bandwidth.  ``per_workload`` times the
+other full-size workloads the same way (graph-replayed step, event-timed
+launches, roofline).  ``cpu_baseline`` times the plain C fp64 oracle on the
+host cores over a bounded sample of the same workload, and ``parity_check``
+compares the timed run's output with the oracle's on that sample.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the step
 (the path has no cross-GPU exchange here); value = all ranks' rows / the
@@ -146,11 +150,14 @@ class Clocks:
         self.t0 = time.time()
 
     def mark(self, begin):
-        """Wall-clock bounds of the timed region (samples outside are dropped)."""
+        """Wall-clock bounds of a timed region (samples outside every region
+        are dropped); call mark(True) / mark(False) around each one."""
+        if not hasattr(self, "regions"):
+            self.regions = []
         if begin:
-            self.r0 = time.time()
-        else:
-            self.r1 = time.time()
+            self.regions.append([time.time(), 1e30])
+        elif self.regions:
+            self.regions[-1][1] = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -162,7 +169,7 @@ class Clocks:
         import datetime
         sm, mx, reasons, total = [], [], set(), 0
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        r0, r1 = getattr(self, "r0", 0.0), getattr(self, "r1", 1e30)
+        regions = getattr(self, "regions", None) or [(getattr(self, "r0", 0.0), getattr(self, "r1", 1e30))]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -173,7 +180,7 @@ class Clocks:
             except ValueError:
                 continue
             total += 1
-            if not (r0 - 0.05 <= ts <= r1 + 0.05):
+            if not any(r0 - 0.05 <= ts <= r1 + 0.05 for r0, r1 in regions):
                 continue
             sm.append(clk)
             mx.append(cmax)
@@ -182,6 +189,125 @@ class Clocks:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples_in_region": len(sm), "samples": total}
+
+
+HEADLINE = "ragged_r256_q8_h12"
+OTHERS = ("decode_r64_h12", "spec_r128_q4_h12", "long_r32_h96p128")
+
+
+class Step:
+    """One workload's device inputs, split plan, buffers and the step's
+    launches (attend, then merge + value/gate)."""
+
+    def __init__(self, spec, args, dev):
+        self.spec, self.args, self.dev = spec, args, dev
+        inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
+        self.inp = inp
+        self.last = inp.extra.get("last_page_len")
+        R, qlen, H = spec.requests, spec.qlen, spec.heads
+        self.S = S = R * qlen
+        ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
+        # Work plan from the host-known lengths (host metadata, like the split
+        # rule): the requests cut so that every CTA gets about the same number
+        # of tiles, at most ns splits each; the partials then need only the
+        # splits the plan used.
+        self.plan_h = None
+        if not args.no_plan:
+            self.plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
+        self.plan = None if self.plan_h is None else self.plan_h.to(dev)
+        self.ns, self.st = ns, st
+        # The query: bf16, or (--q-fp8) e4m3 codes of q * 4 read with q_scale 1/4.
+        self.q_in, self.q_scale = inp.q, 1.0
+        if args.q_fp8:
+            self.q_in, self.q_scale = (inp.q.float() * 4).to(torch.float8_e4m3fn), 0.25
+        self.stats = _plan_stats(inp, ns, st, args.page_size, self.plan_h, self.q_in.element_size())
+        self.o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((ns, S, H), dtype=torch.float32, device=dev)
+        self.latent = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse_m = torch.empty((S, H), dtype=torch.float32, device=dev)
+        self.out = torch.empty((S, H * 128), dtype=torch.bfloat16, device=dev)
+
+    def launch(self, strm, ev=None):
+        a, inp = self.args, self.inp
+        if ev:
+            ev[0].record(strm)
+        mla.attend(self.q_in, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, self.ns, self.st,
+                   heads=inp.heads, qlen=inp.qlen, o=self.o, lse=self.lse, causal=a.causal, page_size=a.page_size,
+                   last_page_len=self.last, plan=self.plan, q_scale=self.q_scale, stream=strm)
+        if ev:
+            ev[1].record(strm)
+        if a.three_call:
+            mla.merge(self.o, self.lse, latent=self.latent, lse_out=self.lse_m, stream=strm)
+            if ev:
+                ev[2].record(strm)
+            mla.value_gate(self.latent, inp.w_uv, inp.gate, inp.lengths, inp.qlen, out=self.out, stream=strm)
+        else:
+            mla.merge_value_gate(self.o, self.lse, inp.w_uv, inp.gate, inp.lengths, inp.qlen, out=self.out,
+                                 latent=self.latent, lse_out=self.lse_m, stream=strm)
+            if ev:
+                ev[2].record(strm)
+        if ev:
+            ev[3].record(strm)
+
+    def warm_and_capture(self, flush, warmup):
+        """Eager warm-up, a status check, then the step captured as one CUDA
+        graph (its launches replayed without host work) and warmed."""
+        stream = torch.cuda.current_stream(self.dev)
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            self.launch(stream)
+        torch.cuda.synchronize(self.dev)
+        flags = mla.device_status()
+        if flags:
+            raise SystemExit("%s: device status flags after warm-up: %#x" % (self.spec.name, flags))
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.launch(torch.cuda.current_stream(self.dev))
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            self.graph.replay()
+        torch.cuda.synchronize(self.dev)
+
+    def time_graph(self, flush, steps):
+        """Seconds per graph-replayed step (L2 flushed before each, outside the events)."""
+        stream = torch.cuda.current_stream(self.dev)
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for k in range(steps):
+            flush.fill_(1.0)
+            gev[k][0].record(stream)
+            self.graph.replay()
+            gev[k][1].record(stream)
+        torch.cuda.synchronize(self.dev)
+        return [e[0].elapsed_time(e[1]) * 1e-3 for e in gev]
+
+    def time_eager(self, flush, steps):
+        """Per-launch seconds (eager launches, an event pair around each)."""
+        stream = torch.cuda.current_stream(self.dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for k in range(steps):
+            flush.fill_(1.0)
+            self.launch(stream, evs[k])
+        torch.cuda.synchronize(self.dev)
+        if mla.device_status():
+            raise SystemExit("%s: device status flags after the timed steps" % self.spec.name)
+        return ([e[0].elapsed_time(e[1]) * 1e-3 for e in evs], [e[1].elapsed_time(e[2]) * 1e-3 for e in evs],
+                [e[2].elapsed_time(e[3]) * 1e-3 for e in evs])
+
+    def kernels_us(self, t_att, t_mrg, t_val):
+        if self.args.three_call:
+            return {"attend": statistics.mean(t_att) * 1e6, "merge": statistics.mean(t_mrg) * 1e6,
+                    "value_gate": statistics.mean(t_val) * 1e6}
+        return {"attend": statistics.mean(t_att) * 1e6, "merge_value_gate": statistics.mean(t_mrg) * 1e6}
+
+    def roofline(self, t_att):
+        hbm, peak_kind = _peaks()
+        att = statistics.mean(t_att)
+        achieved = self.stats["attend_bytes"] / att / 1e9
+        return {"kernel": "attend", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": self.stats["attend_bytes"], "traffic": _ncu_traffic(self.spec.name)}
 
 
 def run_gpu(args):
@@ -193,68 +319,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     mla.build()
     spec = _spec(args.workload)
-    inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
-    last = inp.extra.get("last_page_len")
+    step = Step(spec, args, dev)
+    inp, S, ns, st, plan = step.inp, step.S, step.ns, step.st, step.plan
     R, qlen, H = spec.requests, spec.qlen, spec.heads
-    S = R * qlen
-    ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
-    # Work plan from the host-known lengths (host metadata, like the split
-    # rule above): the requests cut so that every CTA gets about the same
-    # number of tiles, at most ns splits each; the partials then need only
-    # the splits the plan used.
-    plan_h = None
-    if not args.no_plan:
-        plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
-    plan = None if plan_h is None else plan_h.to(dev)
-    # The query: bf16, or (--q-fp8) e4m3 codes of q * 4 read with q_scale 1/4.
-    q_in, q_scale = inp.q, 1.0
-    if args.q_fp8:
-        q_in, q_scale = (inp.q.float() * 4).to(torch.float8_e4m3fn), 0.25
-    stats = _plan_stats(inp, ns, st, args.page_size, plan_h, q_in.element_size())
     stream = torch.cuda.current_stream(dev)
-
-    o = torch.empty((ns, S, H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((ns, S, H), dtype=torch.float32, device=dev)
-    latent = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
-    lse_m = torch.empty((S, H), dtype=torch.float32, device=dev)
-    out = torch.empty((S, H * 128), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step(strm, ev=None):
-        if ev:
-            ev[0].record(strm)
-        mla.attend(q_in, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
-                   o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last, plan=plan,
-                   q_scale=q_scale, stream=strm)
-        if ev:
-            ev[1].record(strm)
-        if args.three_call:
-            mla.merge(o, lse, latent=latent, lse_out=lse_m, stream=strm)
-            if ev:
-                ev[2].record(strm)
-            mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, stream=strm)
-        else:
-            mla.merge_value_gate(o, lse, inp.w_uv, inp.gate, inp.lengths, qlen, out=out, latent=latent, stream=strm)
-            if ev:
-                ev[2].record(strm)
-        if ev:
-            ev[3].record(strm)
-
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step(stream)
-    torch.cuda.synchronize(dev)
-    flags = mla.device_status()
-    if flags:
-        raise SystemExit("device status flags after warm-up: %#x" % flags)
-    # The whole step as one CUDA graph (its launches replayed without host work).
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step(torch.cuda.current_stream(dev))
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        graph.replay()
-    torch.cuda.synchronize(dev)
+    step.warm_and_capture(flush, args.warmup)
 
     clocks = Clocks(local, args.clocks_dir)
     clocks.start()
@@ -262,35 +332,22 @@ def run_gpu(args):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.mark(True)
-    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush.fill_(1.0)
-        gev[k][0].record(stream)
-        graph.replay()
-        gev[k][1].record(stream)
-    torch.cuda.synchronize(dev)
+    t_step = step.time_graph(flush, args.steps)
     clocks.mark(False)
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
-    t_step = [e[0].elapsed_time(e[1]) * 1e-3 for e in gev]
     total = sum(t_step)
-    # Per-launch times (eager launches, an event pair around each).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush.fill_(1.0)
-        step(stream, evs[k])
+    t_att, t_mrg, t_val = step.time_eager(flush, args.steps)
+    # The timed step's outputs, kept for the comparison with the oracle.
+    step.graph.replay()
     torch.cuda.synchronize(dev)
-    t_att = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
-    t_mrg = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
-    t_val = [e[2].elapsed_time(e[3]) * 1e-3 for e in evs]
-    if mla.device_status():
-        raise SystemExit("device status flags after the timed steps")
+    gpu_out = (step.out.cpu(), step.latent.cpu(), step.lse_m.cpu())
 
     # ---- end to end through the public API with host buffers: the step's
     # inputs staged in one pinned host buffer and uploaded with one copy
     # (each piece 256-byte aligned, device views made once), the output read
     # back with one copy.
+    q_in, last, plan_h = step.q_in, step.last, step.plan_h
     host_parts = [q_in, inp.gate, inp.pages, inp.indptr, inp.lengths, last, plan_h]
     offs, total_b = [], 0
     for t in host_parts:
@@ -308,6 +365,7 @@ def run_gpu(args):
         stage_h[off:off + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
         views.append(stage_d[off:off + nb].view(t.dtype).view(t.shape))
     q_d, gate_d, pages_d, indptr_d, lens_d, last_d, plan_d = views
+    out, o, lse, latent, lse_m = step.out, step.o, step.lse, step.latent, step.lse_m
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = total_b
     d2h = out_h.numel() * out_h.element_size()
@@ -316,9 +374,9 @@ def run_gpu(args):
     # these fixed buffers; each step only launches them.
     att = mla.attend(q_d, inp.kv, pages_d, indptr_d, inp.scale, inp.kv_scale, ns, st, heads=H, qlen=qlen,
                      o=o, lse=lse, causal=args.causal, page_size=args.page_size, last_page_len=last_d, plan=plan_d,
-                     q_scale=q_scale, prepare=True)
+                     q_scale=step.q_scale, prepare=True)
     mv = None if args.three_call else mla.merge_value_gate(o, lse, inp.w_uv, gate_d, lens_d, qlen, out=out,
-                                                           latent=latent, prepare=True)
+                                                           latent=latent, lse_out=lse_m, prepare=True)
 
     def e2e_step():
         stage_d.copy_(stage_h, non_blocking=True)
@@ -344,17 +402,37 @@ def run_gpu(args):
         e_t.append(a.elapsed_time(b) * 1e-3)
     e2e_total = sum(e_t)
     ok = torch.equal(out_h, out.cpu())
-    extra = _time_kv_append(inp, S, flush, dev, stream, args.warmup, min(args.steps, 200))
+
+    # ---- the other full-size workloads, each timed the same way (rank 0 of
+    # a single-GPU run only: the scaling runs need the headline alone)
+    per_workload = {}
+    if ws == 1 and not args.no_per_workload and args.workload == HEADLINE:
+        for name in OTHERS:
+            other = Step(_spec(name), args, dev)
+            other.warm_and_capture(flush, args.warmup)
+            clocks.mark(True)
+            ts = other.time_graph(flush, args.steps)
+            clocks.mark(False)
+            oa, om, ov = other.time_eager(flush, args.steps)
+            rl = other.roofline(oa)
+            per_workload[name] = {
+                "requests": other.spec.requests, "qlen": other.spec.qlen, "heads": other.spec.heads,
+                "rows": other.S, "kv_tokens": other.stats["kv_tokens"], "num_splits": other.ns,
+                "ms_per_step": sum(ts) / len(ts) * 1e3, "tokens_per_s": other.S * len(ts) / sum(ts),
+                "kernels_us": other.kernels_us(oa, om, ov),
+                "roofline": {k: rl[k] for k in ("achieved", "peak", "unit", "frac", "algorithmic_bytes_per_launch",
+                                                "traffic")},
+            }
+            del other
+            torch.cuda.empty_cache()
+    clk = clocks.stop()
+    extra = _time_kv_append(S, step.inp.kv_scale, flush, dev, stream, args.warmup, min(args.steps, 200))
 
     if ws > 1:
         total, e2e_total = max_over_ranks([total, e2e_total], dev)
     if rank != 0:
         return None
 
-    hbm, peak_kind = _peaks()
-    att = statistics.mean(t_att)
-    achieved = stats["attend_bytes"] / att / 1e9
-    traffic = _ncu_traffic(spec.name)
     rec = {
         "metric": METRIC,
         "value": aggregate_value(S, args.steps, ws, total),
@@ -370,8 +448,8 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {
             "workload": spec.name, "requests": R, "qlen": qlen, "heads": H, "rows": S,
-            "kv_tokens": stats["kv_tokens"], "kv_bytes": stats["kv_tokens"] * 576,
-            "num_splits": ns, "split_tokens": st if plan is None else None, "work_units": stats["used_units"],
+            "kv_tokens": step.stats["kv_tokens"], "kv_bytes": step.stats["kv_tokens"] * 576,
+            "num_splits": ns, "split_tokens": st if plan is None else None, "work_units": step.stats["used_units"],
             "work_plan": "round robin" if plan is None else "host balanced plan (requests cut at tile boundaries so every CTA gets about the same tiles)",
             "l2": "flushed before every timed step (256 MB write, outside the events)",
             "parallelism": "replicas" if ws > 1 else "single-gpu",
@@ -382,46 +460,44 @@ def run_gpu(args):
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
             "timing": "value: CUDA-graph replay of the step; kernels_us / roofline: eager launches, one event pair each",
         },
-        "kernels_us": ({"attend": att * 1e6, "merge": statistics.mean(t_mrg) * 1e6,
-                        "value_gate": statistics.mean(t_val) * 1e6} if args.three_call else
-                       {"attend": att * 1e6, "merge_value_gate": statistics.mean(t_mrg) * 1e6}),
-        "kv_tokens_per_s": stats["kv_tokens"] * args.steps * ws / total,
-        "roofline": {
-            "kernel": "attend", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
-            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "algorithmic_bytes_per_launch": stats["attend_bytes"], "traffic": traffic,
-        },
+        "kernels_us": step.kernels_us(t_att, t_mrg, t_val),
+        "kv_tokens_per_s": step.stats["kv_tokens"] * args.steps * ws / total,
+        "roofline": step.roofline(t_att),
         "e2e": {"value": aggregate_value(S, args.steps, ws, e2e_total), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "output_matches_device": bool(ok)},
         "gpu_launches": (3 if args.three_call else 2) * args.steps,
         "extra_ops": extra,
         "clocks": clk,
     }
+    if per_workload:
+        rec["per_workload"] = per_workload
     if ws == 1 and not args.no_cpu_baseline:
-        rec["cpu_baseline"] = cpu_baseline(spec, inp)
+        rec["cpu_baseline"], rec["parity_check"] = cpu_baseline(spec, inp, gpu_out=gpu_out, one_thread=True,
+                                                                q_fp8=args.q_fp8, causal=args.causal,
+                                                                page_size=args.page_size)
     return rec
 
 
-def _time_kv_append(inp, S, flush, dev, stream, warmup, steps):
-    """The cache write of new tokens (not part of the timed step): one new
-    token per query row (decode), and a 65,536-token batch (bandwidth).
-    Runs after everything else (it overwrites cache rows)."""
+def _time_kv_append(S, k_scale, flush, dev, stream, warmup, steps):
+    """The cache write of new tokens (not part of the timed step), into a
+    pool of its own (the step's cache is left as it was): one new token per
+    query row (decode), and a 65,536-token batch (bandwidth)."""
     res = {}
-    pool = inp.kv.shape[0]
+    pool = 1 << 17
+    kv = torch.zeros((pool, 576), dtype=torch.uint8, device=dev)
     g = torch.Generator(device=dev).manual_seed(77)
-    for name, T in (("decode_tokens", S), ("batch_65536", min(65536, pool))):
+    for name, T in (("decode_tokens", S), ("batch_65536", 65536)):
         kv_c = torch.randn(T, 512, generator=g, device=dev).to(torch.bfloat16)
         k_pe = torch.randn(T, 64, generator=g, device=dev).to(torch.bfloat16)
         slots = torch.randperm(pool, generator=g, device=dev)[:T].to(torch.int64)
         for _ in range(warmup):
-            mla.kv_append(inp.kv, kv_c, k_pe, slots, inp.kv_scale, stream=stream)
+            mla.kv_append(kv, kv_c, k_pe, slots, k_scale, stream=stream)
         ts = []
         for _ in range(steps):
             flush.fill_(1.0)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            mla.kv_append(inp.kv, kv_c, k_pe, slots, inp.kv_scale, stream=stream)
+            mla.kv_append(kv, kv_c, k_pe, slots, k_scale, stream=stream)
             b.record(stream)
             ts.append((a, b))
         torch.cuda.synchronize(dev)
@@ -466,41 +542,125 @@ def kernel_sources_hash():
     return h.hexdigest()[:16]
 
 
-def cpu_baseline(spec, inp, budget_s=10.0):
-    """Time the plain C fp64 oracle on the host cores on a bounded sample of
-    the workload's requests (the first requests until ~budget_s of work)."""
-    import oracle  # test infrastructure: timed here as the CPU baseline only
-    lib = oracle.load_c()
-    threads = lib.mla_oracle_threads()
-    q = inp.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    kv = inp.kv.cpu().numpy()
-    pages = inp.pages.cpu().numpy()
-    indptr = inp.indptr.cpu().numpy()
-    w = inp.w_uv.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    g = inp.gate.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    lens = np.diff(indptr)
+def _host_cpu():
+    """The host's CPU model (lscpu, else /proc/cpuinfo), core count and OpenMP setting."""
+    model = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                model = v.strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            if k.strip().lower() in ("model name", "cpu model") and v.strip():
+                model = v.strip()
+                break
+    return {"cpu_model": model, "nproc": os.cpu_count(), "omp_num_threads": os.environ.get("OMP_NUM_THREADS")}
+
+
+def _oracle_inputs(inp):
+    """The step's inputs as the C oracle takes them (raw codes and bits)."""
+    return dict(q=inp.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16), kv=inp.kv.cpu().numpy(),
+                pages=inp.pages.cpu().numpy(), indptr=inp.indptr.cpu().numpy(),
+                w=inp.w_uv.cpu().contiguous().view(torch.int16).numpy().view(np.uint16),
+                g=inp.gate.cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _time_oracle(oracle, spec, inp, a, budget_s, threads=0):
+    """Tokens/s of the C oracle over the whole workload, from a bounded
+    sample: requests taken in a seeded random order (a request whose cost
+    alone would take half the budget is passed over) until their estimated
+    cost fills about budget_s on the host's threads, timed and repeated
+    until about the budget is spent, then scaled to the workload by KV
+    tokens (the oracle's work per request is proportional to its context
+    length at fixed rows per request).  Returns (value, threads, sample
+    text, sampled requests, the oracle's outputs)."""
+    lens = np.diff(a["indptr"]).astype(np.int64)
     R = len(lens)
-    # estimate from a one-request probe, then take as many requests as fit the budget
+    nthreads = threads if threads > 0 else oracle.load_c().mla_oracle_threads()
+    nz = np.nonzero(lens > 0)[0]
+    probe_r = int(nz[np.argmin(lens[nz])]) if nz.size else 0
     t0 = time.perf_counter()
-    oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
-                         requests=[0])
-    probe = max(time.perf_counter() - t0, 1e-4)
-    per_token = probe / max(1, lens[0])
-    n = R
-    while n > 1 and per_token * lens[:n].sum() / max(1, min(threads, n)) > budget_s:
-        n = max(1, n // 2)
-    reqs = list(range(n))
+    oracle.decode_step_c(a["q"], a["kv"], a["pages"], a["indptr"], inp.scale, inp.kv_scale, spec.heads, spec.qlen,
+                         a["w"], a["g"], requests=[probe_r], threads=threads)
+    per_token = max(time.perf_counter() - t0, 1e-5) / max(1, lens[probe_r])
+    order = np.random.default_rng(spec.seed).permutation(R)
+    reqs, cost = [], 0.0
+    for r in order:
+        c = per_token * lens[r]
+        if c > 0.5 * budget_s:
+            continue
+        if reqs and (cost + c) / max(1, min(nthreads, len(reqs) + 1)) > budget_s:
+            break
+        reqs.append(int(r))
+        cost += c
+    if not reqs:
+        reqs = [probe_r]
+    reqs.sort()
     reps, t0 = 0, time.perf_counter()
-    while True:   # repeat the sample until about the budget has been spent
-        oracle.decode_step_c(q, kv, pages, indptr, inp.scale, inp.kv_scale, spec.heads, spec.qlen, w, g,
-                             requests=reqs)
+    while True:
+        res = oracle.decode_step_c(a["q"], a["kv"], a["pages"], a["indptr"], inp.scale, inp.kv_scale, spec.heads,
+                                   spec.qlen, a["w"], a["g"], requests=reqs, threads=threads)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or dt / reps * (reps + 1) > 2 * budget_s:
             break
-    return {"value": n * spec.qlen * reps / dt, "unit": UNIT, "cores": int(threads), "kind": "oracle",
-            "sample": "%d of %d requests (%d KV tokens) x %d repetitions, full path in fp64 C, %.2f s" % (
-                n, R, int(lens[:n].sum()), reps, dt)}
+    tok_sample = int(lens[reqs].sum())
+    tok_all = int(lens.sum())
+    t_all = dt / reps * (tok_all / tok_sample if tok_sample > 0 else 1.0)
+    sample = ("%d of %d requests (%d of %d KV tokens, seeded random order) x %d repetitions, full path in fp64 C, "
+              "%.2f s; scaled to the whole workload by KV tokens" % (len(reqs), R, tok_sample, tok_all, reps, dt))
+    return R * spec.qlen / t_all, int(nthreads), sample, reqs, res
+
+
+def cpu_baseline(spec, inp, budget_s=10.0, gpu_out=None, one_thread=False, q_fp8=False, causal=False,
+                 page_size=1):
+    """Time the plain C fp64 oracle on the host cores on a bounded sample of
+    the workload's requests (the first requests until ~budget_s of work).
+    With ``gpu_out`` (out, latent, merged LSE of the timed GPU step, on the
+    CPU) also returns the comparison of those rows with the oracle's; with
+    ``one_thread`` also times one thread on the tiny and the single-token
+    workloads."""
+    import oracle  # test infrastructure: timed here as the CPU baseline only
+    a = _oracle_inputs(inp)
+    value, threads, sample, reqs, res = _time_oracle(oracle, spec, inp, a, budget_s)
+    rec = {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+           "host": _host_cpu(), "build": "gcc -O2 -fopenmp (portable flags, no -march=native)"}
+    if one_thread:
+        rec["one_thread"] = {}
+        for idx, budget in ((0, 2.0), (1, 5.0)):
+            sp = W.WORKLOADS[idx]
+            si = W.make_inputs(sp, "cpu")
+            v, _, smp, _, _ = _time_oracle(oracle, sp, si, _oracle_inputs(si), budget, threads=1)
+            rec["one_thread"][sp.name] = {"value": v, "unit": UNIT, "sample": smp}
+    check = None
+    if gpu_out is not None:
+        if q_fp8 or causal or page_size != 1:
+            check = {"skipped": "the C oracle covers the default step (bf16 query, no mask, page size 1)"}
+        else:
+            rlat, rlse, rout = res
+            rows = np.concatenate([np.arange(r * spec.qlen, (r + 1) * spec.qlen) for r in reqs])
+            g_out, g_lat, g_lse = (t.float().numpy().astype(np.float64)[rows] for t in gpu_out)
+            r_out, r_lat, r_lse = rout[rows], rlat[rows], rlse[rows]
+            err_out = np.abs(g_out - r_out)
+            err_lat = np.abs(g_lat - r_lat)
+            fin = np.isfinite(r_lse)
+            same_inf = bool(np.array_equal(np.isneginf(g_lse), np.isneginf(r_lse)))
+            lse_err = float(np.abs(g_lse[fin] - r_lse[fin]).max()) if fin.any() else 0.0
+            ok_out = bool((err_out <= 2e-2 + 2e-2 * np.abs(r_out)).all())
+            ok_lat = bool((err_lat <= 2e-2 + 2e-2 * np.abs(r_lat)).all())
+            scale_out = float(err_out.max() / max(np.abs(r_out).max(), 1e-300))
+            check = {"requests": len(reqs), "rows": int(len(rows)), "max_abs_err_out": float(err_out.max()),
+                     "max_err_over_max_ref_out": scale_out, "max_abs_err_latent": float(err_lat.max()),
+                     "max_abs_err_lse": lse_err,
+                     "pass": ok_out and ok_lat and same_inf and lse_err <= 1e-3 and scale_out <= 2e-2,
+                     "tolerance": "out / latent |err| <= 2e-2 + 2e-2 |ref| and max|err|/max|ref| <= 2e-2; LSE 1e-3"}
+    return rec, check
 
 
 def run_reference(args):
@@ -512,7 +672,7 @@ def run_reference(args):
     times = []
     base = None
     for k in range(args.warmup + args.steps):
-        res = cpu_baseline(spec, inp, budget_s=args.ref_budget)
+        res, _ = cpu_baseline(spec, inp, budget_s=args.ref_budget)
         if k >= args.warmup:
             times.append(res)
         base = res
@@ -526,7 +686,7 @@ def run_reference(args):
         "config": {"workload": spec.name, "requests": spec.requests, "qlen": spec.qlen, "heads": spec.heads,
                    "rows": S, "note": "each step times the CPU oracle on a bounded sample of the workload"},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
-                         "sample": base["sample"]},
+                         "sample": base["sample"], "host": base["host"]},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -534,11 +694,13 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=W.WORKLOADS[1].name)
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time the chosen workload only (not the other full-size workloads)")
     ap.add_argument("--three-call", action="store_true",
                     help="time merge and value/gate as two launches instead of the fused one")
     ap.add_argument("--ref-budget", type=float, default=5.0)
@@ -561,6 +723,8 @@ def main():
     if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl != "reference":
         import torch.distributed as dist
         dist.destroy_process_group()
+    if rec is not None and rec.get("parity_check") and rec["parity_check"].get("pass") is False:
+        raise SystemExit(3)
 
 
 if __name__ == "__main__":
