@@ -491,7 +491,9 @@ def run_gpu(args):
         "e2e": {"value": aggregate_value(S, args.steps, ws, e2e_total), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "output_matches_device": bool(ok),
                 "pipeline": "two steps in flight: step k+1's upload overlaps step k's kernels, read-back on a "
-                            "second copy stream; buffers alternate between two sets"},
+                            "second copy stream; buffers alternate between two sets",
+                "l2": "not flushed between the overlapped steps: the default workload's KV rows (2.8 GB) exceed L2; "
+                      "on workloads whose KV fits L2 partly, e2e runs L2-warm and can exceed the flushed value"},
         "gpu_launches": (3 if args.three_call else 2) * args.steps,
         "extra_ops": extra,
         "clocks": clk,
