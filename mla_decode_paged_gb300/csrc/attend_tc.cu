@@ -304,15 +304,23 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
     int n_issued = 0;
     const int rows_total = P.qlen * P.heads;
     for (int it = 0; cur.valid; ++it) {
-        // The next unit's query rows into L2 (the softmax converts them when
-        // this unit ends).
+        // The next unit's query rows into L2, kept there against the KV
+        // stream (the softmax converts them when this unit ends): one bulk
+        // prefetch per row, or line prefetches for a row that is not
+        // 16-byte aligned (a row stride that is not a multiple of 8).
         if (pw == kProdWarps - 1 && nxt.valid && (nxt.flags & kTileFirst) && nxt.ntok > 0) {
             const int grp = nxt.flags >> 8;
-            for (int i = lane; i < NQ * 9; i += 32) {
-                const int n = i / 9, line = i - 9 * n, rho = grp * NQ + n;
+            const int esz = P.q8 ? 1 : 2;   // bytes per query element (the row stride counts elements)
+            const uint64_t keep = tc::l2_policy_last();
+            for (int n = lane; n < NQ; n += 32) {
+                const int rho = grp * NQ + n;
                 if (rho < rows_total) {
                     const int tq = rho / P.heads, h = rho - tq * P.heads;
-                    prefetch_l2(P.q + ((int64_t)nxt.r * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK + 64 * line);
+                    const uint8_t *row = reinterpret_cast<const uint8_t *>(P.q) +
+                                         (((int64_t)nxt.r * P.qlen + tq) * P.q_row_stride + (int64_t)h * MLA_D_QK) * esz;
+                    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) tc::bulk_prefetch_l2(row, MLA_D_QK * esz, keep);
+                    else
+                        for (int b = 0; b < MLA_D_QK * esz; b += 128) prefetch_l2(row + b);
                 }
             }
         }
@@ -434,7 +442,7 @@ __device__ void mma_issuer(const PP &P, uint8_t *sm) {
 // c[n] = scale * kv_scale * log2(e).  Run by the 8 softmax warps; a warp
 // copies a 576-byte row as 36 16-byte chunks into the swizzled layouts.
 template <int NQ, class PP>
-__device__ void prep_rows_q8(const PP &P, uint8_t *sm, int req, int grp) {
+__device__ __noinline__ void prep_rows_q8(const PP &P, uint8_t *sm, int req, int grp) {
     using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -470,9 +478,14 @@ __device__ void prep_rows_q8(const PP &P, uint8_t *sm, int req, int grp) {
 // The query rows of tile T's request and row group as the B operand Q':
 // row n = q_n * 2^e_n rounded to e4m3 (hi), row NQ + n = 16 * (q_n * 2^e_n
 // - hi) rounded to e4m3 (lo), in the K-major 128B / 64B swizzled layouts;
-// c[n] = scale * kv_scale * log2(e) / 2^e_n.  Run by the 8 softmax warps.
+// c[n] = scale * kv_scale * log2(e) / 2^e_n.  Run by the 8 softmax warps,
+// out of line (once per unit; up to three of a warp's rows loaded at a
+// time).  At a unit change the query loads wait behind the KV stream
+// (3-4 us on GB300) and the code itself is fetched cold, so this bounds
+// the cost of each unit change; fully unrolled and inlined at its three
+// call sites it measured slower.
 template <int NQ, class PP>
-__device__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
+__device__ __noinline__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
     using C = Cfg<NQ>;
     Misc<NQ> &ms = misc<NQ>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -480,13 +493,14 @@ __device__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
     if (P.q8) {
         prep_rows_q8<NQ>(P, sm, req, grp);
     } else {
-    constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6 rows per warp, all loads in flight at once
-    {
-        constexpr int i0 = 0;
-        uint4 v[kPerWarp][3];
-        bool valid[kPerWarp];
+    constexpr int kPerWarp = NQ / kSoftWarps;   // 2, 4 or 6 rows per warp
+    constexpr int kBatch = kPerWarp % 3 == 0 ? 3 : 2;   // rows whose loads are in flight together
+#pragma unroll 1
+    for (int i0 = 0; i0 < kPerWarp; i0 += kBatch) {
+        uint4 v[kBatch][3];
+        bool valid[kBatch];
 #pragma unroll
-        for (int i = 0; i < kPerWarp; ++i) {
+        for (int i = 0; i < kBatch; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             const int rho = grp * NQ + n;
             valid[i] = rho < rows_total;
@@ -503,7 +517,7 @@ __device__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
             }
         }
 #pragma unroll
-        for (int i = 0; i < kPerWarp; ++i) {
+        for (int i = 0; i < kBatch; ++i) {
             const int n = warp + kSoftWarps * (i0 + i);
             float amax = 0.f;
 #pragma unroll
@@ -606,9 +620,71 @@ __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)
     }
 }
 
+// The end of a unit, once its row sums are in red[] and its reference maxima
+// in m[]: waits for the unit's last P.V, writes each row's LSE (and -inf for
+// the splits past the request's last, k = n_r - 1) and its o rows.  Kept
+// out of line: it runs once per unit, and inlined it only lengthens the
+// per-tile code the instruction cache has to hold.
+template <int NQ, class PP>
+__device__ __noinline__ bool unit_epilogue(const PP &P, uint8_t *sm, int k, int n_r, uint32_t o_parity) {
+    using C = Cfg<NQ>;
+    constexpr int H2 = C::HALF;
+    Misc<NQ> &ms = misc<NQ>(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, wq = warp & 3, t = tid & 127, n0 = (warp >> 2) * H2;
+    const uint32_t tm = ms.tmem + ((uint32_t)(wq * 32) << 16);
+    const int S = P.R * P.qlen;
+    if (!wait_or_abort(&ms.o_done, o_parity, &ms.abort_flag)) return false;
+    tc::fence_after();
+    named_sync(kSoftBar, kSoftThreads);
+    if (tid < NQ) {
+        const float lt = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
+        ms.invl[tid] = lt > 0.f ? P.kv_scale / lt : 0.f;   // a row that saw no token: o = 0
+        const int64_t orow = ms.orow[tid];
+        if (orow >= 0) {
+            P.lse[orow] = (ms.m[tid] + __log2f(lt)) * 0.69314718055994531f;
+            if (k == n_r - 1) {
+                const int64_t step = (int64_t)S * P.heads;
+                for (int k2 = k + 1; k2 < P.num_splits; ++k2) P.lse[orow + (k2 - k) * step] = -INFINITY;
+            }
+        }
+    }
+    named_sync(kSoftBar, kSoftThreads);
+    // o rows: each latent block as bf16 [row][128] in the P' buffer
+    // (idle: this tile's P.V is done), then 16-byte row chunks out.
+    float iv[H2];
+#pragma unroll
+    for (int j = 0; j < H2; ++j) iv[j] = ms.invl[n0 + j];
+    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + C::OffP);
+    // latent blocks staged at a time (4, 2 or 1: a divisor of 4)
+    constexpr int kBlkRound = 4 * NQ * 256 <= C::PBytes ? 4 : 2 * NQ * 256 <= C::PBytes ? 2 : 1;
+#pragma unroll 1
+    for (int b0 = 0; b0 < 4; b0 += kBlkRound) {
+#pragma unroll 1
+        for (int bb = 0; bb < kBlkRound; ++bb) {
+            float hi[H2], lo[H2];
+            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + n0, hi);
+            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + NQ + n0, lo);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < H2; ++j)
+                stg[(bb * NQ + n0 + j) * 128 + t] = __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * iv[j]);
+        }
+        named_sync(kSoftBar, kSoftThreads);
+        for (int c = tid; c < kBlkRound * NQ * 16; c += kSoftThreads) {
+            const int row = c >> 4, ch = c & 15, bb = row / NQ, n = row - bb * NQ;
+            const int64_t orow = ms.orow[n];
+            if (orow >= 0)
+                *reinterpret_cast<uint4 *>(P.o + orow * MLA_D_LATENT + 128 * (b0 + bb) + 8 * ch) =
+                    *reinterpret_cast<const uint4 *>(stg + row * 128 + 8 * ch);
+        }
+        named_sync(kSoftBar, kSoftThreads);
+    }
+    return true;
+}
+
 // Softmax warpgroups: thread (warpgroup g, TMEM lane t) owns token t of the
 // tile (latent row t of O in the epilogue) and query columns
-// [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale), c/16 and
+// [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale) and
 // the reference max m in registers.  The tile sequence comes from the
 // stage descriptors.  CAUSAL compiles the causal mask in (a separate
 // instantiation, so the unmasked path carries none of its work).
@@ -621,7 +697,7 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
     const int wq = warp & 3, t = tid & 127, n0 = (warp >> 2) * H2;
     const uint32_t tm = ms.tmem + ((uint32_t)(wq * 32) << 16);
     const int S = P.R * P.qlen, rows_total = P.qlen * P.heads;
-    float l[H2], cr[H2], c16[H2], mr[H2];
+    float l[H2], cr[H2], mr[H2];
     int n_s = 0, n_units = 0;
     int vmin = 0;   // causal: tokens of the request every query row sees (L_r - qlen + 1)
     uint8_t *prow = sm + C::OffP + (t >> 3) * 1024 + (t & 7) * 128;
@@ -657,7 +733,6 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
             for (int j = 0; j < H2; ++j) {
                 l[j] = 0.f;
                 cr[j] = ms.c[n0 + j];
-                c16[j] = cr[j] * 0.0625f;
                 mr[j] = -INFINITY;
             }
             if (tid < NQ) {
@@ -693,14 +768,14 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
             if (!mask_tile) {
 #pragma unroll
                 for (int j = 0; j < H2; ++j) {
-                    sc[j] = live ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                    sc[j] = live ? cr[j] * fmaf(lo[j], 0.0625f, hi[j]) : -INFINITY;
                     over |= sc[j] - mr[j] > kRebase;   // also true for every live token while m = -inf
                 }
             } else {
                 const int pos = M.tok0 + t;   // token position in the request
 #pragma unroll
                 for (int j = 0; j < H2; ++j) {
-                    sc[j] = live && pos < ms.vis[n0 + j] ? fmaf(hi[j], cr[j], lo[j] * c16[j]) : -INFINITY;
+                    sc[j] = live && pos < ms.vis[n0 + j] ? cr[j] * fmaf(lo[j], 0.0625f, hi[j]) : -INFINITY;
                     over |= sc[j] - mr[j] > kRebase;
                 }
             }
@@ -783,52 +858,7 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
                     for (int j = 0; j < H2; ++j) ms.m[n0 + j] = mr[j];
                 }
             }
-            if (!wait_or_abort(&ms.o_done, n_units & 1, &ms.abort_flag)) return;
-            tc::fence_after();
-            named_sync(kSoftBar, kSoftThreads);
-            if (tid < NQ) {
-                const float lt = ms.red[0][tid] + ms.red[1][tid] + ms.red[2][tid] + ms.red[3][tid];
-                ms.invl[tid] = lt > 0.f ? P.kv_scale / lt : 0.f;   // a row that saw no token: o = 0
-                const int64_t orow = ms.orow[tid];
-                if (orow >= 0) {
-                    P.lse[orow] = (ms.m[tid] + __log2f(lt)) * 0.69314718055994531f;
-                    if (M.k == M.n_r - 1) {
-                        const int64_t step = (int64_t)S * P.heads;
-                        for (int k2 = M.k + 1; k2 < P.num_splits; ++k2) P.lse[orow + (k2 - M.k) * step] = -INFINITY;
-                    }
-                }
-            }
-            named_sync(kSoftBar, kSoftThreads);
-            // o rows: each latent block as bf16 [row][128] in the P' buffer
-            // (idle: this tile's P.V is done), then 16-byte row chunks out.
-            float iv[H2];
-#pragma unroll
-            for (int j = 0; j < H2; ++j) iv[j] = ms.invl[n0 + j];
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + C::OffP);
-            // latent blocks staged at a time (4, 2 or 1: a divisor of 4)
-            constexpr int kBlkRound = 4 * NQ * 256 <= C::PBytes ? 4 : 2 * NQ * 256 <= C::PBytes ? 2 : 1;
-#pragma unroll 1
-            for (int b0 = 0; b0 < 4; b0 += kBlkRound) {
-#pragma unroll 1
-                for (int bb = 0; bb < kBlkRound; ++bb) {
-                    float hi[H2], lo[H2];
-                    ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + n0, hi);
-                    ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + NQ + n0, lo);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < H2; ++j)
-                        stg[(bb * NQ + n0 + j) * 128 + t] = __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * iv[j]);
-                }
-                named_sync(kSoftBar, kSoftThreads);
-                for (int c = tid; c < kBlkRound * NQ * 16; c += kSoftThreads) {
-                    const int row = c >> 4, ch = c & 15, bb = row / NQ, n = row - bb * NQ;
-                    const int64_t orow = ms.orow[n];
-                    if (orow >= 0)
-                        *reinterpret_cast<uint4 *>(P.o + orow * MLA_D_LATENT + 128 * (b0 + bb) + 8 * ch) =
-                            *reinterpret_cast<const uint4 *>(stg + row * 128 + 8 * ch);
-                }
-                named_sync(kSoftBar, kSoftThreads);
-            }
+            if (!unit_epilogue<NQ>(P, sm, M.k, M.n_r, n_units & 1)) return;
             tc::fence_before();
             ++n_units;
         }

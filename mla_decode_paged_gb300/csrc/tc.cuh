@@ -43,6 +43,20 @@ __device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
     return p;
 }
 
+// L2 cache policy for data that should outlast the surrounding stream.
+__device__ __forceinline__ uint64_t l2_policy_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 with a cache policy (src
+// 16-byte aligned, bytes a multiple of 16); nothing is written anywhere.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 // Swizzle modes of the UMMA shared-memory descriptor.
 constexpr uint32_t kSw128 = 2, kSw64 = 4;
 
