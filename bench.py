@@ -193,26 +193,42 @@ class Clocks:
 
 HEADLINE = "ragged_r256_q8_h12"
 OTHERS = ("decode_r64_h12", "spec_r128_q4_h12", "long_r32_h96p128")
+# The speculative-decode workload's description cuts every request into 8 to
+# 32 split-KV partials: 32 splits of 512 tokens under the split rule do that
+# for its U[4096, 32768] contexts.
+STATED_CUT = ("spec_r128_q4_h12", (32, 512))
+
+
+def _parse_splits(text):
+    """``"NS:ST"`` -> (num_splits, split_tokens), or None."""
+    if not text:
+        return None
+    ns, st = (int(x) for x in text.split(":"))
+    if ns < 1 or st < 1:
+        raise SystemExit("--splits wants two positive integers NS:ST")
+    return ns, st
 
 
 class Step:
     """One workload's device inputs, split plan, buffers and the step's
     launches (attend, then merge + value/gate)."""
 
-    def __init__(self, spec, args, dev):
+    def __init__(self, spec, args, dev, splits=None):
         self.spec, self.args, self.dev = spec, args, dev
+        splits = splits or _parse_splits(args.splits)
         inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
         self.inp = inp
         self.last = inp.extra.get("last_page_len")
         R, qlen, H = spec.requests, spec.qlen, spec.heads
         self.S = S = R * qlen
-        ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu())
+        ns, st = mla.choose_splits(R, qlen, H, lengths=inp.lengths.cpu()) if splits is None else splits
         # Work plan from the host-known lengths (host metadata, like the split
         # rule): the requests cut so that every CTA gets about the same number
         # of tiles, at most ns splits each; the partials then need only the
-        # splits the plan used.
+        # splits the plan used.  A given (num_splits, split_tokens) is timed
+        # under the split rule itself.
         self.plan_h = None
-        if not args.no_plan:
+        if not args.no_plan and splits is None:
             self.plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
         self.plan = None if self.plan_h is None else self.plan_h.to(dev)
         self.ns, self.st = ns, st
@@ -448,6 +464,27 @@ def run_gpu(args):
                 "roofline": {k: rl[k] for k in ("achieved", "peak", "unit", "frac", "algorithmic_bytes_per_launch",
                                                 "traffic")},
             }
+            if name == STATED_CUT[0]:
+                # the same workload cut the way its description states (every
+                # request into 8-32 partials, split rule), timed the same way
+                del other
+                torch.cuda.empty_cache()
+                other = Step(_spec(name), args, dev, splits=STATED_CUT[1])
+                other.warm_and_capture(flush, args.warmup)
+                clocks.mark(True)
+                ts = other.time_graph(flush, args.steps)
+                clocks.mark(False)
+                oa, om, ov = other.time_eager(flush, args.steps)
+                rl = other.roofline(oa)
+                lens = other.inp.lengths.cpu().long()
+                n_r = torch.clamp((lens + other.st - 1) // other.st, 1, other.ns)
+                per_workload[name]["stated_cut"] = {
+                    "num_splits": other.ns, "split_tokens": other.st, "work_plan": "none (split rule)",
+                    "partials_per_request": [int(n_r.min()), int(n_r.max())],
+                    "ms_per_step": sum(ts) / len(ts) * 1e3, "tokens_per_s": other.S * len(ts) / sum(ts),
+                    "kernels_us": other.kernels_us(oa, om, ov),
+                    "roofline": {k: rl[k] for k in ("achieved", "frac", "algorithmic_bytes_per_launch")},
+                }
             del other
             torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -739,6 +776,8 @@ def main():
                     help="fp8 e4m3 query codes (q * 4) with q_scale 1/4 instead of the bf16 query")
     ap.add_argument("--no-plan", action="store_true",
                     help="round-robin work units under the split rule instead of the host work plan")
+    ap.add_argument("--splits", default=None, metavar="NS:ST",
+                    help="num_splits:split_tokens under the split rule (no work plan) instead of the host plan")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     ap.add_argument("--clocks-dir", default=None,

@@ -339,6 +339,31 @@ def test_full_size_workloads_every_request(idx, kernel, capsys):
     assert mla.device_status() == 0
 
 
+def test_speculative_workload_with_8_to_32_partials(kernel, capsys):
+    """The speculative-decode workload cut the way its description states:
+    every request into 8 to 32 split-KV partials (split rule, 32 splits of
+    512 tokens), then the LSE merge and W_UV + gate.  Merged results of every
+    request against the oracle (the same reference as any other cut); the
+    partials of sampled requests against the oracle's per-split attention."""
+    idx = 2
+    inp = W.make_inputs(idx, DEV)
+    ns, st = 32, 512
+    lens = i32(inp.lengths)
+    n_r = np.minimum(ns, np.maximum(1, -(-lens // st)))
+    assert n_r.min() >= 8 and n_r.max() <= 32
+    o, lse, latent, lse_m, out = _run_path(inp, ns, st, kernel)
+    ref = F.reference(("plain", idx), inp)
+    F.check_every_row("%s, 8-32 partials (%s kernel)" % (inp.spec.name, kernel), ref, latent, lse_m, out, capsys)
+    inp_cpu = _to(inp, "cpu")   # the same bytes (a CPU generator would draw others)
+    reqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17, 64})
+    ro, rl = O.attend_splits(**oracle_args(inp_cpu), num_splits=ns, split_tokens=st, requests=reqs)
+    rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
+    sel = torch.from_numpy(rows).to(DEV)
+    assert_lse_close(lse[:, sel], rl[:, rows], "partial lse (8-32 partials)")
+    assert_bf16_close(o[:, sel], ro[:, rows], "partial o (8-32 partials)", mask=np.isfinite(rl[:, rows]))
+    assert mla.device_status() == 0
+
+
 # ------------------------------------------------------------- causal option
 
 CAUSAL_SMALL = [
