@@ -339,28 +339,30 @@ def test_full_size_workloads_every_request(idx, kernel, capsys):
     assert mla.device_status() == 0
 
 
-def test_speculative_workload_with_8_to_32_partials(kernel, capsys):
-    """The speculative-decode workload cut the way its description states:
-    every request into 8 to 32 split-KV partials (split rule, 32 splits of
-    512 tokens), then the LSE merge and W_UV + gate.  Merged results of every
-    request against the oracle (the same reference as any other cut); the
-    partials of sampled requests against the oracle's per-split attention."""
-    idx = 2
+@pytest.mark.parametrize("idx,ns,st,lo,hi", [(2, 32, 512, 8, 32), (3, 16, 2048, 16, 16)])
+def test_workloads_at_their_stated_split_counts(idx, ns, st, lo, hi, kernel, capsys):
+    """Workloads cut the way their descriptions state, under the split rule:
+    the speculative-decode one into 8 to 32 split-KV partials per request
+    (32 splits of 512 tokens), the 96-head long-context one into 16 (heavy
+    split-KV: 16 splits of 2,048 tokens); then the LSE merge and W_UV + gate.
+    Merged results of every request against the oracle (the same reference
+    as any other cut); the partials of sampled requests against the oracle's
+    per-split attention."""
     inp = W.make_inputs(idx, DEV)
-    ns, st = 32, 512
     lens = i32(inp.lengths)
     n_r = np.minimum(ns, np.maximum(1, -(-lens // st)))
-    assert n_r.min() >= 8 and n_r.max() <= 32
+    assert n_r.min() >= lo and n_r.max() <= hi
     o, lse, latent, lse_m, out = _run_path(inp, ns, st, kernel)
     ref = F.reference(("plain", idx), inp)
-    F.check_every_row("%s, 8-32 partials (%s kernel)" % (inp.spec.name, kernel), ref, latent, lse_m, out, capsys)
+    F.check_every_row("%s, %d-%d partials (%s kernel)" % (inp.spec.name, n_r.min(), n_r.max(), kernel), ref, latent,
+                      lse_m, out, capsys)
     inp_cpu = _to(inp, "cpu")   # the same bytes (a CPU generator would draw others)
-    reqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17, 64})
+    reqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17, len(lens) - 1})
     ro, rl = O.attend_splits(**oracle_args(inp_cpu), num_splits=ns, split_tokens=st, requests=reqs)
     rows = np.concatenate([np.arange(r * inp.qlen, (r + 1) * inp.qlen) for r in reqs])
     sel = torch.from_numpy(rows).to(DEV)
-    assert_lse_close(lse[:, sel], rl[:, rows], "partial lse (8-32 partials)")
-    assert_bf16_close(o[:, sel], ro[:, rows], "partial o (8-32 partials)", mask=np.isfinite(rl[:, rows]))
+    assert_lse_close(lse[:, sel], rl[:, rows], "partial lse (stated split count)")
+    assert_bf16_close(o[:, sel], ro[:, rows], "partial o (stated split count)", mask=np.isfinite(rl[:, rows]))
     assert mla.device_status() == 0
 
 
