@@ -54,6 +54,7 @@ constexpr int kSoftWarps = 8, kMmaWarp = 8, kProdWarp0 = 9, kProdWarps = 7;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kThreads = (kSoftWarps + 1 + kProdWarps) * 32;
 constexpr int kSoftBar = 1;          // named barrier of the two softmax warpgroups
+constexpr int kGroupBar = 2;         // 2 + g: named barrier of softmax warpgroup g alone
 constexpr float kRebase = 8.f;       // log2 headroom before the reference max moves
 
 // Tile shape and shared-memory layout per row count NQ: two 128-token
@@ -780,8 +781,11 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
                 }
             }
         }
-        // ---- lazy reference max (rare after a unit's first tile)
-        if (tc::bar_any(kSoftBar, kSoftThreads, over)) {
+        // ---- lazy reference max (rare after a unit's first tile).  A
+        // warpgroup's columns are its own, so the vote and the rebase stay
+        // within the warpgroup.
+        const bool g1 = warp >= 4;
+        if (g1 ? tc::bar_any(kGroupBar + 1, 128, over) : tc::bar_any(kGroupBar, 128, over)) {
 #pragma unroll
             for (int j = 0; j < H2; ++j) {
                 float v = sc[j];
@@ -789,15 +793,18 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
                 for (int dd = 16; dd; dd >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, dd));
                 if (lane == 0) ms.red[wq][n0 + j] = v;
             }
-            named_sync(kSoftBar, kSoftThreads);
-            if (tid < NQ) {
-                const float mo = first ? -INFINITY : ms.m[tid];
-                float mn = fmaxf(fmaxf(ms.red[0][tid], ms.red[1][tid]), fmaxf(ms.red[2][tid], ms.red[3][tid]));
+            if (g1) named_sync(kGroupBar + 1, 128);
+            else named_sync(kGroupBar, 128);
+            if (t < H2) {
+                const int n = n0 + t;
+                const float mo = first ? -INFINITY : ms.m[n];
+                float mn = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
                 mn = fmaxf(mn, mo);
-                ms.alpha[tid] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-                ms.m[tid] = mn;
+                ms.alpha[n] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+                ms.m[n] = mn;
             }
-            named_sync(kSoftBar, kSoftThreads);
+            if (g1) named_sync(kGroupBar + 1, 128);
+            else named_sync(kGroupBar, 128);
 #pragma unroll
             for (int j = 0; j < H2; ++j) {
                 mr[j] = ms.m[n0 + j];
