@@ -8,15 +8,15 @@
 // sigmoid of the raw gate, rounded to bf16; rows of empty requests are 0,
 // chosen by a select so a NaN gate never leaks).
 //
-// Design: one CTA per (64 query rows, head), 128 threads.  The head's whole
+// Design: one CTA per (64 query rows, head), 512 threads.  The head's whole
 // W_UV slice [128 x 512] and the 64 latent rows [64 x 512] arrive by TMA in
 // one round trip, K-major with 128B swizzle (eight 64-element column blocks
 // each); they are the A (M = 128 output columns) and B (N = 64 rows)
 // operands of 32 bf16 tcgen05 MMAs (K = 16) issued by one thread into a
-// 64-column f32 TMEM accumulator D[v][row].  The epilogue reads D (thread =
-// output column v = TMEM lane), rounds the value to bf16 into a shared
-// [64][128] tile, then writes each row's 128 outputs with coalesced 4-byte
-// stores (the gate words, loaded the same way, are in flight during the
+// 64-column f32 TMEM accumulator D[v][row].  The epilogue reads D (four
+// warps, thread = output column v = TMEM lane), rounds the value to bf16
+// into a shared [64][128] tile, then all 16 warps write each row's 128
+// outputs with coalesced 4-byte stores (the gate words, loaded the same way, are in flight during the
 // copies and MMAs).  The W_UV slice is read before the wait on
 // the previous kernel (programmatic dependent launch); the latent, gate and
 // lengths after it.
@@ -31,7 +31,7 @@ namespace mla {
 namespace {
 
 constexpr int kRows = 64;                                  // query rows per CTA (MMA N)
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;                              // warps 0-3 read TMEM; all write
 constexpr int kColBlocks = MLA_D_LATENT / 64;              // 128-byte column blocks of the K axis
 constexpr int kABlock = MLA_D_V * 128;                     // one column block of W_UV[h]: 16 KB
 constexpr int kBBlock = kRows * 128;                       // one column block of the latent rows: 8 KB
@@ -65,7 +65,14 @@ __device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x,
         : "memory");
 }
 
-__device__ __forceinline__ float sigmoid_f32(float x) { return 1.f / (1.f + expf(-x)); }
+// 1 / (1 + e^-x) in fp32 from the hardware exponential and reciprocal
+// approximations (relative errors near 2^-21 and 2^-23, far below the bf16
+// rounding of the product); e^-x = inf gives 0.
+__device__ __forceinline__ float sigmoid_f32(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + __expf(-x)));
+    return r;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     value_gate_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap ml,
@@ -149,16 +156,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
 
     // D[v][row] -> bf16(value) in a [64][128] tile (the W_UV slice is no
-    // longer read: its first 16 KB hold the tile).
+    // longer read: its first 16 KB hold the tile); warps 0-3 cover the 128
+    // TMEM lanes.
     __nv_bfloat16 *tile = reinterpret_cast<__nv_bfloat16 *>(sm + kAOff);
-    const int v = 32 * warp + lane;
+    if (warp < 4) {
+        const int v = 32 * warp + lane;
 #pragma unroll
-    for (int c = 0; c < kRows; c += 16) {
-        float d[16];
-        tc::ld16(tm + ((uint32_t)(32 * warp) << 16) + c, d);
-        tc::wait_ld();
+        for (int c = 0; c < kRows; c += 16) {
+            float d[16];
+            tc::ld16(tm + ((uint32_t)(32 * warp) << 16) + c, d);
+            tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) tile[(c + i) * MLA_D_V + v] = __float2bfloat16_rn(d[i]);
+            for (int i = 0; i < 16; ++i) tile[(c + i) * MLA_D_V + v] = __float2bfloat16_rn(d[i]);
+        }
     }
     tc::fence_before();
     __syncthreads();
@@ -200,29 +210,51 @@ cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *
                               const int32_t *lengths, int R, int qlen, int H, void *out, cudaStream_t st) {
     const int S = R * qlen;
     if (S == 0) return cudaSuccess;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
     // W_UV as [H*128 rows, 512] and the latent as [S][H][512], 64-element
-    // (128-byte) boxes with 128B swizzle: the UMMA K-major layout.
-    CUtensorMap mw, ml;
-    {
-        cuuint64_t dim[2] = {(cuuint64_t)MLA_D_LATENT, (cuuint64_t)H * MLA_D_V};
-        cuuint64_t stride[1] = {(cuuint64_t)MLA_D_LATENT * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)MLA_D_V}, es[2] = {1, 1};
-        if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_uv), dim, stride, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+    // (128-byte) boxes with 128B swizzle: the UMMA K-major layout.  Encoded
+    // once per (device, buffer, shape) and reused while a thread keeps
+    // launching on the same buffers.
+    struct MapCache {
+        int dev;
+        const void *ptr;
+        int S, H;
+        CUtensorMap map;
+    };
+    static thread_local MapCache cw = {-1, nullptr, 0, 0, {}}, cl = {-1, nullptr, 0, 0, {}};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (cw.dev != dev || cw.ptr != w_uv || cw.H != H || cl.dev != dev || cl.ptr != latent || cl.S != S || cl.H != H) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+        if (!enc) return cudaErrorNotSupported;
+        if (cw.dev != dev || cw.ptr != w_uv || cw.H != H) {
+            cw.dev = -1;
+            cuuint64_t dim[2] = {(cuuint64_t)MLA_D_LATENT, (cuuint64_t)H * MLA_D_V};
+            cuuint64_t stride[1] = {(cuuint64_t)MLA_D_LATENT * 2};
+            cuuint32_t box[2] = {64, (cuuint32_t)MLA_D_V}, es[2] = {1, 1};
+            if (enc(&cw.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_uv), dim, stride, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+            cw.dev = dev;
+            cw.ptr = w_uv;
+            cw.H = H;
+        }
+        if (cl.dev != dev || cl.ptr != latent || cl.S != S || cl.H != H) {
+            cl.dev = -1;
+            cuuint64_t dim[3] = {(cuuint64_t)MLA_D_LATENT, (cuuint64_t)H, (cuuint64_t)S};
+            cuuint64_t stride[2] = {(cuuint64_t)MLA_D_LATENT * 2, (cuuint64_t)H * MLA_D_LATENT * 2};
+            cuuint32_t box[3] = {64, 1, (cuuint32_t)kRows}, es[3] = {1, 1, 1};
+            if (enc(&cl.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(latent), dim, stride, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+            cl.dev = dev;
+            cl.ptr = latent;
+            cl.S = S;
+            cl.H = H;
+        }
     }
-    {
-        cuuint64_t dim[3] = {(cuuint64_t)MLA_D_LATENT, (cuuint64_t)H, (cuuint64_t)S};
-        cuuint64_t stride[2] = {(cuuint64_t)MLA_D_LATENT * 2, (cuuint64_t)H * MLA_D_LATENT * 2};
-        cuuint32_t box[3] = {64, 1, (cuuint32_t)kRows}, es[3] = {1, 1, 1};
-        if (enc(&ml, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(latent), dim, stride, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    const CUtensorMap &mw = cw.map, &ml = cl.map;
     cudaError_t e = smem_attr_once<value_gate_kernel>(kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
