@@ -245,6 +245,11 @@ mla_status mla_decode_attend_planned(const void *q, int64_t q_row_stride, const 
  *   o        bf16 [num_splits, rows, heads, 512]; lse f32 [num_splits, rows, heads]
  *   latent   bf16 [rows, heads, 512] (written)
  *   lse_out  f32  [rows, heads] (written; may be NULL)
+ *
+ * A kernel enqueued after this call with programmatic dependent launch may
+ * start while the merge runs; it must wait for the grid dependency
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads
+ * latent or lse_out, as mla_value_gate does.
  */
 mla_status mla_merge_splits(const void *o, const float *lse, int num_splits, int rows,
                             int heads, void *latent, float *lse_out, void *stream);
@@ -265,6 +270,14 @@ mla_status mla_merge_splits(const void *o, const float *lse, int num_splits, int
  *   latent   bf16 [S, heads, 512];  w_uv bf16 [heads, 128, 512]
  *   gate     bf16 [S, heads*128] (raw logits);  lengths int32 [num_requests]
  *   out      bf16 [S, heads*128] (written);  S = num_requests * qlen
+ *
+ * The sum runs on the tensor cores (fp32 accumulation, in the hardware's
+ * order); the sigmoid uses the hardware exponential and reciprocal
+ * approximations (relative error below 1e-6, far under the bf16 rounding).
+ * The kernel starts reading w_uv before the kernel enqueued just before it
+ * on the stream has finished (programmatic dependent launch; latent, gate
+ * and lengths are read after that kernel completes): w_uv must not be
+ * written by that kernel.
  */
 mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate,
                           const int32_t *lengths, int num_requests, int qlen, int heads,
@@ -274,9 +287,11 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
  * mla_merge_value_gate -- mla_merge_splits followed by mla_value_gate in one
  * call.  Small batches (at most half as many 16-row tiles x heads as SMs)
  * run as a single launch that forms the merged latent in shared memory and
- * projects and gates it straight away; larger ones run the two kernels.
- * Both routes give the same bytes as the two calls (the latent is rounded
- * to bf16 before the projection).
+ * projects and gates it straight away (warp-level MMAs); larger ones run the
+ * two kernels.  Both routes give the same latent and LSE bytes as the two
+ * calls (the latent is rounded to bf16 before the projection); out can
+ * differ from the two calls' in the last bf16 place on the one-launch route
+ * (its fp32 sums run in a different order).
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
  * m1c_inputs / post (the LSE merge of the splits, then W_UV and the gate)
@@ -288,8 +303,8 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
  *   latent               bf16 [S, heads, 512] (written: the merged latent)
  *   lse_out              f32 [S, heads] (written; may be NULL)
  *
- * The one-launch route starts reading w_uv before the kernel enqueued just
- * before it on the stream has finished (programmatic dependent launch; every
+ * Both routes start reading w_uv before the kernel enqueued just before
+ * them on the stream has finished (programmatic dependent launch; every
  * other input is read after that kernel completes): w_uv must not be
  * written by that kernel.
  */

@@ -32,6 +32,10 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const __nv_bfloat16 
                                                             int num_splits, long long nrow,
                                                             __nv_bfloat16 *__restrict__ latent,
                                                             float *__restrict__ lse_out) {
+    // A kernel launched after this one with programmatic dependent launch
+    // (the W_UV + gate kernel) may start now; it waits for this grid's
+    // completion before it reads what this kernel writes.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (row >= nrow) return;
