@@ -338,9 +338,18 @@ int mla_choose_splits(int num_requests, int qlen, int heads, int max_len, int64_
 
 namespace {
 
-// Cost model of the work plan, in tenths of a 128-token tile: a tile, the
-// fixed share of a split (query prep, epilogue) and an empty request.
-constexpr int64_t kPlanTile = 10, kPlanPiece = 5, kPlanEmpty = 2;
+// Cost model of the work plan, in tenths of a 128-token tile: a tile and an
+// empty request; plan_piece_cost gives the fixed cost of a split.
+constexpr int64_t kPlanTile = 10, kPlanEmpty = 2;
+
+// The fixed cost of a split (a unit change in the kernel: the next unit's
+// query converted, the finished unit's o and LSE written, the first tile's
+// rebase) for nq query rows per CTA.  Measured on GB300 with clock stamps
+// at 48 rows, ~25,000-30,000 cycles against a ~4,700-cycle tile; costed
+// here at 3 tiles for 48 rows, 1.5 for 32 and half a tile for 16 (the
+// settings that measured fastest in attend A/Bs of the plan: at 48 rows 3
+// tiles beat 0.5, 2 and 5; at 16 rows 0.5 beat 2 and 3).
+int64_t plan_piece_cost(int nq) { return nq >= 48 ? 30 : nq >= 32 ? 15 : 5; }
 
 struct PlanPiece {
     int r, k, start, count;
@@ -351,7 +360,7 @@ struct PlanPiece {
 // boundaries where a CTA fills up.  Returns the CTAs used (V + 1 when more
 // than V would be needed or a request would need more than max_splits
 // pieces); pieces are appended per CTA when `out` is given.
-int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_splits,
+int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_splits, int64_t piece,
               std::vector<std::vector<PlanPiece>> *out) {
     int v = 0;
     int64_t load = 0;
@@ -371,12 +380,12 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
         int done = 0, k = 0;
         while (done < ntiles) {
             const int64_t room = budget - load;
-            if (load > 0 && room < kPlanPiece + kPlanTile) {
+            if (load > 0 && room < piece + kPlanTile) {
                 if (++v >= V) return V + 1;
                 load = 0;
                 continue;
             }
-            int64_t take = (room - kPlanPiece) / kPlanTile;
+            int64_t take = (room - piece) / kPlanTile;
             if (take < 1) take = 1;
             if (take > ntiles - done) take = ntiles - done;
             if (++k > max_splits) return V + 1;
@@ -385,7 +394,7 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
                 const int count = (int)std::min<int64_t>((int64_t)take * 128, (int64_t)L - start);
                 (*out)[v].push_back({r, k - 1, start, count});
             }
-            load += take * kPlanTile + kPlanPiece;
+            load += take * kPlanTile + piece;
             done += (int)take;
         }
     }
@@ -427,20 +436,21 @@ int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_le
     // tiles at about the same time.
     const int V = sm_count / groups;
     if (V < 1) return fail(MLA_ERR_UNSUPPORTED, "fewer SMs than query-row groups");
+    const int64_t piece = plan_piece_cost(nq);
     // Smallest budget whose fill fits V CTAs within num_splits pieces per
     // request (the fill with an unbounded budget always fits: one CTA, one
     // piece per request).
     int64_t total = 0;
     for (int r = 0; r < num_requests; ++r)
-        total += host_lengths[r] > 0 ? ((host_lengths[r] + 127) / 128) * kPlanTile + kPlanPiece : kPlanEmpty;
-    int64_t lo = 0, hi = total + kPlanPiece + kPlanTile;
+        total += host_lengths[r] > 0 ? ((host_lengths[r] + 127) / 128) * kPlanTile + piece : kPlanEmpty;
+    int64_t lo = 0, hi = total + piece + kPlanTile;
     while (hi - lo > 1) {
         const int64_t mid = lo + (hi - lo) / 2;
-        if (plan_fill(host_lengths, num_requests, mid, V, num_splits, nullptr) <= V) hi = mid;
+        if (plan_fill(host_lengths, num_requests, mid, V, num_splits, piece, nullptr) <= V) hi = mid;
         else lo = mid;
     }
     std::vector<std::vector<PlanPiece>> vc;
-    plan_fill(host_lengths, num_requests, hi, V, num_splits, &vc);
+    plan_fill(host_lengths, num_requests, hi, V, num_splits, piece, &vc);
     // pieces per request (n_r) and the plan's size
     std::vector<int> n_r(num_requests > 0 ? num_requests : 1, 1);
     int64_t items = 0;

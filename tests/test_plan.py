@@ -16,7 +16,7 @@ from tests import _plan
 
 NULL = ctypes.c_void_p(0)
 P16 = ctypes.c_void_p(1 << 20)   # never dereferenced: each case below fails validation first
-TILE, PIECE, EMPTY = 10, 5, 2    # the planner's cost model, tenths of a 128-token tile
+TILE, EMPTY = 10, 2    # the planner's cost model, tenths of a 128-token tile
 
 
 @pytest.fixture(scope="module")
@@ -29,8 +29,17 @@ def _groups(qlen, heads):
     return -(-qlen * heads // 48)
 
 
-def _cost(count):
-    return (-(-count // 128)) * TILE + PIECE if count > 0 else EMPTY
+def _piece(qlen, heads):
+    """The planner's fixed cost of a split for the CTA's query-row tile
+    (3 tiles at 48 rows, 1.5 at 32, half a tile at 16)."""
+    rows = qlen * heads
+    g = -(-rows // 48)
+    nq = -(-(-(-rows // g)) // 16) * 16
+    return 30 if nq >= 48 else 15 if nq >= 32 else 5
+
+
+def _cost(count, piece=5):
+    return (-(-count // 128)) * TILE + piece if count > 0 else EMPTY
 
 
 CASES = [
@@ -84,9 +93,10 @@ def test_plan_balance_within_a_tile_of_the_mean(lengths, qlen, heads, ns, G):
     g = _groups(qlen, heads)
     V = G // g
     _, off, it = _plan.items(plan)
-    loads = [sum(_cost(c) for c in it[off[v * g]:off[v * g + 1], 5]) for v in range(V)]
-    per_split = max([-(-(-(-L // 128)) // ns) * TILE + PIECE for L in lengths if L > 0] or [0])
-    assert max(loads) <= max(sum(loads) / (V - 1), per_split) + TILE + PIECE
+    piece = _piece(qlen, heads)
+    loads = [sum(_cost(c, piece) for c in it[off[v * g]:off[v * g + 1], 5]) for v in range(V)]
+    per_split = max([-(-(-(-L // 128)) // ns) * TILE + piece for L in lengths if L > 0] or [0])
+    assert max(loads) <= max(sum(loads) / (V - 1), per_split) + TILE + piece
 
 
 def test_plan_by_hand_without_cuts():
