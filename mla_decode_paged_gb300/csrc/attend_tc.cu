@@ -481,10 +481,9 @@ __device__ __noinline__ void prep_rows_q8(const PP &P, uint8_t *sm, int req, int
 // - hi) rounded to e4m3 (lo), in the K-major 128B / 64B swizzled layouts;
 // c[n] = scale * kv_scale * log2(e) / 2^e_n.  Run by the 8 softmax warps,
 // out of line (once per unit; up to three of a warp's rows loaded at a
-// time).  At a unit change the query loads wait behind the KV stream
-// (3-4 us on GB300) and the code itself is fetched cold, so this bounds
-// the cost of each unit change; fully unrolled and inlined at its three
-// call sites it measured slower.
+// time).  At a unit change its conversion work and its code, fetched
+// cold, bound the cost of the change; fully unrolled and inlined at its
+// three call sites it measured slower.
 template <int NQ, class PP>
 __device__ __noinline__ void prep_query(const PP &P, uint8_t *sm, int req, int grp) {
     using C = Cfg<NQ>;
