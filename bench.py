@@ -518,7 +518,7 @@ def run_gpu(args):
             "kv": "fp8-e4m3 paged (page size %d%s)" % (args.page_size, ", block tables" if args.page_size > 1 else ""),
             "mask": "causal within a request" if args.causal else "none",
             "query": "fp8 e4m3 codes of q * 4, q_scale 1/4" if args.q_fp8 else "bf16",
-            "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 -> f32 tcgen05 (W_UV; mma.sync in the fused small-batch merge + W_UV)",
+            "mma": "e4m3 x e4m3 -> f32 tcgen05 (attend, two-term split), bf16 -> f32 tcgen05 (W_UV, both merge routes)",
             "launches_per_step": "attend, merge+value/gate" if not args.three_call else "attend, merge, value/gate",
             "timing": "value: CUDA-graph replay of the step; kernels_us / roofline: eager launches, one event pair each",
         },

@@ -285,13 +285,12 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
 
 /*
  * mla_merge_value_gate -- mla_merge_splits followed by mla_value_gate in one
- * call.  Small batches (at most half as many 16-row tiles x heads as SMs)
- * run as a single launch that forms the merged latent in shared memory and
- * projects and gates it straight away (warp-level MMAs); larger ones run the
- * two kernels.  Both routes give the same latent and LSE bytes as the two
- * calls (the latent is rounded to bf16 before the projection); out can
- * differ from the two calls' in the last bf16 place on the one-launch route
- * (its fp32 sums run in a different order).
+ * call.  Small batches (at most twice as many 16-row tiles x heads as SMs)
+ * run as a single launch that merges 16 rows of a head, writes them, and
+ * projects and gates them straight from shared memory (the same tensor-core
+ * MMAs as mla_value_gate); larger ones run the two kernels.  Both routes
+ * give the same latent, LSE and out bytes as the two calls (the latent is
+ * rounded to bf16 before the projection).
  *
  * Defined by: vllm.models.kimi_k3.amd.specialized_decode.runtime.mla,
  * m1c_inputs / post (the LSE merge of the splits, then W_UV and the gate)

@@ -37,8 +37,7 @@ cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *
 cudaError_t value_gate_status(unsigned int *flags, bool clear);
 cudaError_t merge_value_launch(const void *o, const float *lse, int num_splits, const void *w_uv, const void *gate,
                                const int32_t *lengths, int R, int qlen, int H, void *out, void *latent,
-                               float *lse_out, int sms, cudaStream_t st);
-cudaError_t merge_value_status(unsigned int *flags, bool clear);
+                               float *lse_out, cudaStream_t st);
 cudaError_t gather_launch(const void *kv, int64_t pool_rows, const int32_t *pages, const int32_t *indptr,
                           int R, int64_t total_rows, void *out, cudaStream_t st);
 cudaError_t gather_status(unsigned int *flags, bool clear);
@@ -250,12 +249,15 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
     const int64_t S = (int64_t)num_requests * qlen;
     cudaError_t e;
-    if (((S + 15) / 16) * heads <= sms / 2) {
+    // One launch while its 16-row CTAs (one per SM at a time) number at most
+    // two waves; past that, loading the head's 128 KB W_UV slice per 16 rows
+    // costs more than the separate merge and the 64-row value kernel save.
+    // Graph-replayed steps on one GB300: 64 x 12 rows (48 CTAs) and 32 x 96
+    // (192) are faster fused, 512 x 12 (384) and 2,048 x 12 (1,536) split.
+    if (((S + 15) / 16) * heads <= 2 * (int64_t)sms) {
         e = mla::merge_value_launch(o, lse, num_splits, w_uv, gate, lengths, num_requests, qlen, heads, out, latent,
-                                    lse_out, sms, st);
+                                    lse_out, st);
     } else {
-        // Larger batches: a fused kernel would re-read every partial row
-        // once per column block; the two kernels read each once.
         e = mla::merge_launch(o, lse, num_splits, (int)S, heads, latent, lse_out, st);
         if (e == cudaSuccess)
             e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out, st);
@@ -539,7 +541,7 @@ mla_status mla_device_status(void *stream, unsigned int *flags) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     cudaError_t (*readers[])(unsigned int *, bool) = {mla::attend_mma_status, mla::attend_tc_status, mla::merge_status,
-                                                      mla::value_gate_status, mla::gather_status, mla::merge_value_status,
+                                                      mla::value_gate_status, mla::gather_status,
                                                       mla::kv_append_status};
     for (auto rd : readers) {
         unsigned int f = 0;

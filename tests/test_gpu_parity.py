@@ -244,9 +244,9 @@ def test_value_gate_standalone(R, qlen, heads):
 @pytest.mark.parametrize("idx,lengths", SMALL)
 def test_fused_merge_value_matches_oracle_and_two_call_path(idx, lengths):
     """mla_merge_value_gate and merge followed by value_gate, each against the
-    oracle; their merged latent and LSE byte-equal (the same merge
-    arithmetic; the W_UV products come from different MMA paths, so `out`
-    is compared through the oracle)."""
+    oracle, and byte-equal to each other: both routes merge with the same row
+    function and run the same 32 bf16 tensor-core MMAs (K = 16, in the same
+    order) and the same sigmoid, only with 16 or 64 rows per MMA."""
     inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
     inp = _to(inp_cpu, DEV)
     o, lse, latent, lse_m, out = _run_path(inp, 4, 40)
@@ -258,6 +258,7 @@ def test_fused_merge_value_matches_oracle_and_two_call_path(idx, lengths):
     _check_full(latent, lse_m, out, inp_cpu)
     assert torch.equal(lat2, latent)
     assert torch.equal(torch.nan_to_num(lse2, neginf=-1e30), torch.nan_to_num(lse_m, neginf=-1e30))
+    assert torch.equal(out2, out)
 
 
 @pytest.mark.parametrize("splits,R,qlen,heads", [(1, 3, 1, 12), (6, 70, 1, 12), (9, 40, 8, 12), (3, 2, 1, 96),
