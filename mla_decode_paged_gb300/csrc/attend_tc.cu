@@ -581,9 +581,10 @@ __device__ __noinline__ void prep_query(const PP &P, uint8_t *sm, int req, int g
 
 // p = 2^(s - m) of a thread's H2 scores, added to the row sums l and split
 // into e4m3 hi + lo/16 (hi = p rounded to 3 mantissa bits in fp32, exact in
-// e4m3; lo = 16 * (p - hi)), packed four columns per word.  GUARD maps
-// s = -inf to 0 even where m is still -inf (causal tiles; without the mask
-// every column sees each tile's live tokens, so m is finite by then).
+// e4m3; lo = 16 * (p - hi)), packed four columns per word.  REL: sc holds
+// s - m already (the unmasked kernel).  GUARD maps s = -inf to 0 even where
+// m is still -inf (causal tiles; without the mask every column sees each
+// tile's live tokens, so m is finite by then).
 // 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative
 // error ~2^-22, results below 2^-126 flushed to 0).  p is then rounded to
 // two e4m3 terms (~8 significant bits), so the approximation is invisible
@@ -594,7 +595,7 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
-template <int H2, bool GUARD>
+template <int H2, bool GUARD, bool REL>
 __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)[H2], float (&l)[H2],
                                         uint32_t (&ph)[H2 / 4], uint32_t (&pl)[H2 / 4]) {
 #pragma unroll
@@ -602,7 +603,8 @@ __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)
         float hv[2], lv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2_approx(sc[j + e] - mr[j + e]) : 0.f;
+            const float x = REL ? sc[j + e] : sc[j + e] - mr[j + e];   // REL: sc already holds s - m
+            const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2_approx(x) : 0.f;
             l[j + e] += pv;
             hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
             lv[e] = (pv - hv[e]) * 16.f;
@@ -733,7 +735,7 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
             for (int j = 0; j < H2; ++j) {
                 l[j] = 0.f;
                 cr[j] = ms.c[n0 + j];
-                mr[j] = -INFINITY;
+                mr[j] = CAUSAL ? -INFINITY : 0.f;
             }
             if (tid < NQ) {
                 const int rho = grp * NQ + tid;
@@ -765,7 +767,23 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
             ld_cols<H2>(tm + NQ + n0, lo);
             tc::wait_ld();
             const bool live = t < M.ntok;
-            if (!mask_tile) {
+            if constexpr (!CAUSAL) {
+                // Unmasked: scores kept relative to the reference max, s - m,
+                // with m folded into the scaling FMA.  A unit's first tile
+                // runs with m = 0 (so sc = s) and always votes; every column
+                // sees that tile's live tokens, so m is finite after it.
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < H2; ++j) {
+                        sc[j] = fmaf(cr[j], fmaf(lo[j], 0.0625f, hi[j]), -mr[j]);
+                        over |= sc[j] > kRebase;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < H2; ++j) sc[j] = -INFINITY;
+                }
+                over |= first;
+            } else if (!mask_tile) {
 #pragma unroll
                 for (int j = 0; j < H2; ++j) {
                     sc[j] = live ? cr[j] * fmaf(lo[j], 0.0625f, hi[j]) : -INFINITY;
@@ -796,17 +814,31 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
             else named_sync(kGroupBar, 128);
             if (t < H2) {
                 const int n = n0 + t;
-                const float mo = first ? -INFINITY : ms.m[n];
-                float mn = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
-                mn = fmaxf(mn, mo);
-                ms.alpha[n] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-                ms.m[n] = mn;
+                const float mx = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
+                if constexpr (!CAUSAL) {
+                    // mx is the tile's largest s (first tile) or s - m.
+                    if (first) {
+                        ms.alpha[n] = 0.f;
+                        ms.m[n] = mx;
+                    } else {
+                        const float d = fmaxf(mx, 0.f);
+                        ms.alpha[n] = exp2f(-d);
+                        ms.m[n] += d;
+                    }
+                } else {
+                    const float mo = first ? -INFINITY : ms.m[n];
+                    const float mn = fmaxf(mx, mo);
+                    ms.alpha[n] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+                    ms.m[n] = mn;
+                }
             }
             if (g1) named_sync(kGroupBar + 1, 128);
             else named_sync(kGroupBar, 128);
 #pragma unroll
             for (int j = 0; j < H2; ++j) {
-                mr[j] = ms.m[n0 + j];
+                const float mn = ms.m[n0 + j];
+                if constexpr (!CAUSAL) sc[j] -= mn - mr[j];   // now s - (new m); mr = 0 on a first tile
+                mr[j] = mn;
                 l[j] *= ms.alpha[n0 + j];
             }
             if (!first) {
@@ -833,8 +865,9 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
         // mantissa bits in fp32 (exact in e4m3), lo = 16 * (p - hi); this
         // thread's bytes of row t of P'^T
         uint32_t ph[H2 / 4], pl[H2 / 4];
-        if (!mask_tile) p_split<H2, false>(sc, mr, l, ph, pl);
-        else p_split<H2, true>(sc, mr, l, ph, pl);   // masked entries: 0 even while a column's m is -inf
+        if constexpr (!CAUSAL) p_split<H2, false, true>(sc, mr, l, ph, pl);
+        else if (!mask_tile) p_split<H2, false, false>(sc, mr, l, ph, pl);
+        else p_split<H2, true, false>(sc, mr, l, ph, pl);   // masked entries: 0 even while a column's m is -inf
         if (C::T == 128 || t < C::T) {   // lanes past a shorter tile have no P' row
 #pragma unroll
             for (int g = 0; g < H2 / 8; ++g) {
