@@ -23,7 +23,9 @@
 //     as the B operand's 2*NQ rows, so one MMA chain yields both partial
 //     scores (an fp8 query is used as one exact term).  P.V:
 //     O^T[lat, n] = V^T[lat, tok] . P'^T[tok, n], with the same smem bytes
-//     read MN-major as V^T and P likewise split into hi + lo/16.
+//     read MN-major as V^T and P likewise split into hi + lo (p taken
+//     against a reference 4 below the running max, so lo ~ p/16 stays in
+//     e4m3's normal range).
 //     kind::f8f6f4 E4M3 x E4M3 with f32 accumulation in TMEM:
 //     S' at columns [0, 2NQ), O' for latent block b at [2NQ(1+b), 2NQ(2+b)).
 //   * warp 8 (MMA): one thread issues 18 QK MMAs (K = 32 each) and, once P
@@ -56,6 +58,7 @@ constexpr int kThreads = (kSoftWarps + 1 + kProdWarps) * 32;
 constexpr int kSoftBar = 1;          // named barrier of the two softmax warpgroups
 constexpr int kGroupBar = 2;         // 2 + g: named barrier of softmax warpgroup g alone
 constexpr float kRebase = 8.f;       // log2 headroom before the reference max moves
+constexpr float kRefGap = 4.f;       // a rebase puts the reference this far (log2) below the new max
 
 // Tile shape and shared-memory layout per row count NQ: two 128-token
 // stages.  (The layout also admits shorter tiles -- a 96-token tile still
@@ -580,11 +583,15 @@ __device__ __noinline__ void prep_query(const PP &P, uint8_t *sm, int req, int g
 }
 
 // p = 2^(s - m) of a thread's H2 scores, added to the row sums l and split
-// into e4m3 hi + lo/16 (hi = p rounded to 3 mantissa bits in fp32, exact in
-// e4m3; lo = 16 * (p - hi)), packed four columns per word.  REL: sc holds
-// s - m already (the unmasked kernel).  GUARD maps s = -inf to 0 even where
-// m is still -inf (causal tiles; without the mask every column sees each
-// tile's live tokens, so m is finite by then).
+// into e4m3 hi + lo (hi = p rounded to 3 mantissa bits in fp32, exact in
+// e4m3; lo = p - hi), packed four columns per word.  The reference m sits
+// kRefGap = 4 below the largest score seen when it was last moved, so p is
+// at most 16 then and below 2^kRebase until the next move: 16 times the
+// max-referenced probability, which keeps lo (~p/16) in e4m3's normal range
+// as far down as the max-referenced p = 2^-6.  REL (the unmasked kernel): sc
+// holds s - m already.  GUARD maps s = -inf to 0 even where m is still -inf
+// (causal tiles; without the mask every column sees each tile's live tokens,
+// so m is finite by then).
 // 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative
 // error ~2^-22, results below 2^-126 flushed to 0).  p is then rounded to
 // two e4m3 terms (~8 significant bits), so the approximation is invisible
@@ -607,7 +614,7 @@ __device__ __forceinline__ void p_split(const float (&sc)[H2], const float (&mr)
             const float pv = (!GUARD || sc[j + e] > -INFINITY) ? exp2_approx(x) : 0.f;
             l[j + e] += pv;
             hv[e] = __uint_as_float((__float_as_uint(pv) + 0x80000u) & 0xFFF00000u);
-            lv[e] = (pv - hv[e]) * 16.f;
+            lv[e] = pv - hv[e];
         }
         const uint32_t h8 = __nv_cvt_float2_to_fp8x2(make_float2(hv[0], hv[1]), __NV_SATFINITE, __NV_E4M3);
         const uint32_t l8 = __nv_cvt_float2_to_fp8x2(make_float2(lv[0], lv[1]), __NV_SATFINITE, __NV_E4M3);
@@ -669,7 +676,7 @@ __device__ __noinline__ bool unit_epilogue(const PP &P, uint8_t *sm, int k, int 
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < H2; ++j)
-                stg[(bb * NQ + n0 + j) * 128 + t] = __float2bfloat16_rn((hi[j] + lo[j] * 0.0625f) * iv[j]);
+                stg[(bb * NQ + n0 + j) * 128 + t] = __float2bfloat16_rn((hi[j] + lo[j]) * iv[j]);
         }
         named_sync(kSoftBar, kSoftThreads);
         for (int c = tid; c < kBlkRound * NQ * 16; c += kSoftThreads) {
@@ -687,7 +694,8 @@ __device__ __noinline__ bool unit_epilogue(const PP &P, uint8_t *sm, int k, int 
 // Softmax warpgroups: thread (warpgroup g, TMEM lane t) owns token t of the
 // tile (latent row t of O in the epilogue) and query columns
 // [g*NQ/2, (g+1)*NQ/2).  Per column it keeps c (the score scale) and
-// the reference max m in registers.  The tile sequence comes from the
+// the reference m in registers (kRefGap below the running max).  The tile
+// sequence comes from the
 // stage descriptors.  CAUSAL compiles the causal mask in (a separate
 // instantiation, so the unmasked path carries none of its work).
 template <int NQ, bool CAUSAL, class PP>
@@ -816,18 +824,20 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
                 const int n = n0 + t;
                 const float mx = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
                 if constexpr (!CAUSAL) {
-                    // mx is the tile's largest s (first tile) or s - m.
+                    // mx is the tile's largest s (first tile) or s - m; the
+                    // reference goes kRefGap below the new max (p <= 16 after
+                    // a rebase, < 2^kRebase before the next).
                     if (first) {
                         ms.alpha[n] = 0.f;
-                        ms.m[n] = mx;
+                        ms.m[n] = mx - kRefGap;
                     } else {
-                        const float d = fmaxf(mx, 0.f);
+                        const float d = fmaxf(mx - kRefGap, 0.f);
                         ms.alpha[n] = exp2f(-d);
                         ms.m[n] += d;
                     }
                 } else {
                     const float mo = first ? -INFINITY : ms.m[n];
-                    const float mn = fmaxf(mx, mo);
+                    const float mn = fmaxf(mx - kRefGap, mo);   // stays -inf for a column with no visible token
                     ms.alpha[n] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
                     ms.m[n] = mn;
                 }
@@ -845,25 +855,46 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
                 // O holds this unit's earlier tiles (their P.V is complete:
                 // this tile's QK^T was issued after it): scale this
                 // warpgroup's hi and lo columns of every latent block.
+                if constexpr (NQ == 32) {
+                    // Eight columns at a time: this kernel's register
+                    // allocation spills on this rare path otherwise.
 #pragma unroll 1
-                for (int b = 0; b < 4; ++b) {
-#pragma unroll 1
-                    for (int part = 0; part < 2; ++part) {
-                        float v[H2];
-                        const uint32_t addr = tm + C::NP * (1 + b) + part * NQ + n0;
-                        ld_cols<H2>(addr, v);
-                        tc::wait_ld();
+                    for (int c = 0; c < H2; c += 8) {
+                        float a[8];
 #pragma unroll
-                        for (int j = 0; j < H2; ++j) v[j] *= ms.alpha[n0 + j];
-                        st_cols<H2>(addr, v);
+                        for (int i = 0; i < 8; ++i) a[i] = ms.alpha[n0 + c + i];
+#pragma unroll 1
+                        for (int bp = 0; bp < 8; ++bp) {
+                            float v[8];
+                            const uint32_t addr = tm + C::NP * (1 + (bp >> 1)) + (bp & 1) * NQ + n0 + c;
+                            ld_cols<8>(addr, v);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] *= a[i];
+                            st_cols<8>(addr, v);
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int b = 0; b < 4; ++b) {
+#pragma unroll 1
+                        for (int part = 0; part < 2; ++part) {
+                            float v[H2];
+                            const uint32_t addr = tm + C::NP * (1 + b) + part * NQ + n0;
+                            ld_cols<H2>(addr, v);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int j = 0; j < H2; ++j) v[j] *= ms.alpha[n0 + j];
+                            st_cols<H2>(addr, v);
+                        }
                     }
                 }
                 tc::wait_st();
             }
         }
-        // ---- P' = hi + lo/16 of p = 2^(s - m) (<= 2^8): hi = p rounded to 3
-        // mantissa bits in fp32 (exact in e4m3), lo = 16 * (p - hi); this
-        // thread's bytes of row t of P'^T
+        // ---- P' = hi + lo of p = 2^(s - m) (<= 2^8): hi = p rounded to 3
+        // mantissa bits in fp32 (exact in e4m3), lo = p - hi; this thread's
+        // bytes of row t of P'^T
         uint32_t ph[H2 / 4], pl[H2 / 4];
         if constexpr (!CAUSAL) p_split<H2, false, true>(sc, mr, l, ph, pl);
         else if (!mask_tile) p_split<H2, false, false>(sc, mr, l, ph, pl);

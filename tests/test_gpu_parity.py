@@ -569,6 +569,54 @@ def test_fp8_query_full_size_every_request(capsys):
     assert mla.device_status() == 0
 
 
+# ------------------------------------------- rising scores (reference moves)
+
+def _rising_keys(inp_cpu, gain=100.0):
+    """The workload's KV rows with their 64 rope values (key only: the value
+    is the 512 latent values) scaled by 1 + (gain - 1) * pos / L inside each
+    request (page size 1), so each 128-token tile's largest score lies far
+    above every earlier tile's: the kernel's lazy reference max moves, and the
+    O accumulated so far is rescaled, on most tiles of a unit, while the
+    values keep their ordinary size."""
+    kv = inp_cpu.kv.view(torch.float8_e4m3fn).float()
+    pages, indptr = inp_cpu.pages.long(), inp_cpu.indptr.long()
+    for r in range(len(indptr) - 1):
+        rows = pages[indptr[r]:indptr[r + 1]]
+        n = len(rows)
+        if n:
+            g = 1.0 + (gain - 1.0) * torch.arange(n, dtype=torch.float32) / max(n - 1, 1)
+            kv[rows, 512:] *= g[:, None]
+    inp_cpu.kv = kv.to(torch.float8_e4m3fn).view(torch.uint8)
+    return inp_cpu
+
+
+@pytest.mark.parametrize("idx,lengths", [(1, [1, 200, 1000, 2000]), (2, [700, 1500]), (4, [0, 300, 1200])])
+@pytest.mark.parametrize("mode", ["split rule", "plan", "causal"])
+def test_rising_scores_move_the_reference_and_match_oracle(idx, lengths, mode, kernel, capsys):
+    if kernel == "mma" and mode != "split rule":
+        pytest.skip("the warp-MMA cross-check kernel takes no work plan and no mask")
+    inp_cpu = _rising_keys(W.make_inputs(idx, "cpu", lengths=lengths))
+    inp = _to(inp_cpu, DEV)
+    ns, st, kw = 3, 512, {}
+    if mode == "plan":
+        plan_h, ns = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 4)
+        kw["plan"] = plan_h.to(DEV)
+    if mode == "causal":
+        kw["causal"] = True
+    o, lse = _attend(kernel, inp.q, inp.kv, inp.pages, inp.indptr, inp.scale, inp.kv_scale, ns, st,
+                     heads=inp.heads, qlen=inp.qlen, **kw)
+    latent, lse_m = mla.merge(o, lse)
+    out = mla.value_gate(latent, inp.w_uv, inp.gate, inp.lengths, inp.qlen)
+    torch.cuda.synchronize()
+    a = oracle_args(inp_cpu)
+    rlat, rlse, rout = O.decode_step(**a, w_uv_bits=bf16_bits(inp_cpu.w_uv), gate_bits=bf16_bits(inp_cpu.gate),
+                                     lengths=i32(inp_cpu.lengths), causal=mode == "causal")
+    assert np.nanmax(np.abs(rlse[np.isfinite(rlse)])) > 20      # scores far beyond the first tile's
+    F.check_every_row("%s rising scores (%s, %s)" % (inp.spec.name, kernel, mode), (rlat, rlse, rout), latent,
+                      lse_m, out, capsys)
+    assert mla.device_status() == 0
+
+
 # ------------------------------------------------------ outlier-channel query
 
 def _outlier_query(inp_cpu, rope_gain=64.0, chan_gain=100.0, chans=(7, 100, 300)):
