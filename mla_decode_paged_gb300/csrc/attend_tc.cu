@@ -27,7 +27,9 @@
 //     against a reference 4 below the running max, so lo ~ p/16 stays in
 //     e4m3's normal range).
 //     kind::f8f6f4 E4M3 x E4M3 with f32 accumulation in TMEM:
-//     S' at columns [0, 2NQ), O' for latent block b at [2NQ(1+b), 2NQ(2+b)).
+//     S' at columns [0, 2NQ) (all hi, then all lo), O' for latent block b at
+//     [2NQ(1+b), 2NQ(2+b)) in P' order (per softmax warpgroup: the hi terms
+//     of its query columns, then their lo terms).
 //   * warp 8 (MMA): one thread issues 18 QK MMAs (K = 32 each) and, once P
 //     is in smem, 16 PV MMAs per tile; tcgen05.commit releases the stage.
 //   * warps 0..7 (softmax, two warpgroups, thread = TMEM lane = token, each
@@ -671,8 +673,8 @@ __device__ __noinline__ bool unit_epilogue(const PP &P, uint8_t *sm, int k, int 
 #pragma unroll 1
         for (int bb = 0; bb < kBlkRound; ++bb) {
             float hi[H2], lo[H2];
-            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + n0, hi);
-            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + NQ + n0, lo);
+            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + 2 * n0, hi);   // P' column order: see softmax
+            ld_cols<H2>(tm + C::NP * (1 + b0 + bb) + 2 * n0 + H2, lo);
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < H2; ++j)
@@ -866,7 +868,7 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
 #pragma unroll 1
                         for (int bp = 0; bp < 8; ++bp) {
                             float v[8];
-                            const uint32_t addr = tm + C::NP * (1 + (bp >> 1)) + (bp & 1) * NQ + n0 + c;
+                            const uint32_t addr = tm + C::NP * (1 + (bp >> 1)) + 2 * n0 + (bp & 1) * H2 + c;
                             ld_cols<8>(addr, v);
                             tc::wait_ld();
 #pragma unroll
@@ -880,7 +882,7 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
 #pragma unroll 1
                         for (int part = 0; part < 2; ++part) {
                             float v[H2];
-                            const uint32_t addr = tm + C::NP * (1 + b) + part * NQ + n0;
+                            const uint32_t addr = tm + C::NP * (1 + b) + 2 * n0 + part * H2;
                             ld_cols<H2>(addr, v);
                             tc::wait_ld();
 #pragma unroll
@@ -900,11 +902,20 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
         else if (!mask_tile) p_split<H2, false, false>(sc, mr, l, ph, pl);
         else p_split<H2, true, false>(sc, mr, l, ph, pl);   // masked entries: 0 even while a column's m is -inf
         if (C::T == 128 || t < C::T) {   // lanes past a shorter tile have no P' row
+            // P' columns are ordered by warpgroup, [hi of its H2 columns, lo
+            // of them]: this thread's 2*H2 bytes of row t start at 2*n0 and
+            // fill H2/8 whole 16-byte swizzle chunks (one store each).
+            uint32_t w[H2 / 2];
 #pragma unroll
-            for (int g = 0; g < H2 / 8; ++g) {
-                const int bh = n0 + 8 * g, bl = NQ + n0 + 8 * g;   // byte offsets in the 128-byte row
-                *reinterpret_cast<uint2 *>(prow + ((((bh >> 4) ^ t) & 7) << 4) + (bh & 15)) = make_uint2(ph[2 * g], ph[2 * g + 1]);
-                *reinterpret_cast<uint2 *>(prow + ((((bl >> 4) ^ t) & 7) << 4) + (bl & 15)) = make_uint2(pl[2 * g], pl[2 * g + 1]);
+            for (int i = 0; i < H2 / 4; ++i) {
+                w[i] = ph[i];
+                w[H2 / 4 + i] = pl[i];
+            }
+#pragma unroll
+            for (int q = 0; q < H2 / 8; ++q) {
+                const int chunk = 2 * n0 / 16 + q;
+                *reinterpret_cast<uint4 *>(prow + (((chunk ^ t) & 7) << 4)) =
+                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
         }
         tc::fence_async_smem();
