@@ -547,12 +547,16 @@ __device__ __noinline__ void prep_query(const PP &P, uint8_t *sm, int req, int g
                 uint32_t hi[2], lo[2];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
+                    // lo = 16 (x - hi) in f16x2, exactly: x (a bf16 value times
+                    // a power of two, |x| < 256) and hi are f16 values, x - hi
+                    // is exact (hi is x rounded to e4m3), and so is the x16.
                     const float2 x = make_float2(bf16_lo(w[e2]) * sc, bf16_hi(w[e2]) * sc);
                     const __nv_fp8x2_storage_t h8 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
                     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                    const float2 r = make_float2((x.x - hf.x) * 16.f, (x.y - hf.y) * 16.f);
-                    const __nv_fp8x2_storage_t l8 = __nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+                    const __half2 r = __hmul2(__hsub2(__float22half2_rn(x), *reinterpret_cast<const __half2 *>(&hr)),
+                                              __float2half2_rn(16.f));
+                    const __nv_fp8x2_storage_t l8 =
+                        __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw *>(&r), __NV_SATFINITE, __NV_E4M3);
                     if ((e2 & 1) == 0) {
                         hi[e2 >> 1] = h8;
                         lo[e2 >> 1] = l8;
