@@ -347,11 +347,12 @@ constexpr int64_t kPlanTile = 10, kPlanEmpty = 2;
 // The fixed cost of a split (a unit change in the kernel: the next unit's
 // query converted, the finished unit's o and LSE written, the first tile's
 // rebase) for nq query rows per CTA.  Measured on GB300 with clock stamps
-// at 48 rows, ~25,000-30,000 cycles against a ~4,700-cycle tile; costed
-// here at 3 tiles for 32 and 48 rows and half a tile for 16, the settings
-// that measured fastest in attend A/Bs of the plan (at 48 rows 3 tiles beat
-// 0.5, 2 and 5; at 32 rows 3 beat 0.5 and 1.5; at 16 rows 0.5 beat 2 and 3).
-int64_t plan_piece_cost(int nq) { return nq >= 32 ? 30 : 5; }
+// at 48 rows, ~18,500 cycles against a ~4,600-cycle tile; costed here at 4
+// tiles for 48 rows, 3 for 32 and half a tile for 16, the settings that
+// measured fastest in attend A/Bs of the plan (at 48 rows 4 tiles beat 3 and
+// 5, and earlier 3 beat 0.5, 2 and 5; at 32 rows 3 beat 0.5 and 1.5; at 16
+// rows 0.5 beat 1.5, 2.5 and 3).
+int64_t plan_piece_cost(int nq) { return nq >= 48 ? 40 : nq >= 32 ? 30 : 5; }
 
 struct PlanPiece {
     int r, k, start, count;

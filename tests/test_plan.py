@@ -31,11 +31,11 @@ def _groups(qlen, heads):
 
 def _piece(qlen, heads):
     """The planner's fixed cost of a split for the CTA's query-row tile
-    (3 tiles at 32 and 48 rows, half a tile at 16)."""
+    (4 tiles at 48 rows, 3 at 32, half a tile at 16)."""
     rows = qlen * heads
     g = -(-rows // 48)
     nq = -(-(-(-rows // g)) // 16) * 16
-    return 30 if nq >= 32 else 5
+    return 40 if nq >= 48 else 30 if nq >= 32 else 5
 
 
 def _cost(count, piece=5):
