@@ -223,7 +223,9 @@ def test_merge_standalone(splits, rows, heads):
 
 
 @pytest.mark.parametrize("R,qlen,heads", [(3, 1, 12), (70, 1, 12), (5, 4, 12), (9, 8, 12), (2, 1, 96), (1, 3, 5),
-                                          (33, 4, 12), (3, 1, 128), (40, 5, 3)])
+                                          (33, 4, 12), (3, 1, 128), (40, 5, 3),
+                                          # the persistent kernel: several 32-row tiles per CTA, ragged last tile
+                                          (250, 8, 12), (45, 3, 64), (1100, 1, 12)])
 def test_value_gate_standalone(R, qlen, heads):
     S = R * qlen
     lat = W.make_latent(S, heads, seed=R)
