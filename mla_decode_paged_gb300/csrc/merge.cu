@@ -2,8 +2,9 @@
 //
 // What it computes: vLLM API page
 // vllm.models.kimi_k3.amd.specialized_decode.runtime.mla -- m1c_inputs
-// (partials o [splits, S, H, 512] bf16, LSE [splits, S, H] f32, "M1b
-// merges the splits") and post (the same LSE combine across ranks):
+// (partials o [splits, S, H, 512] bf16 and LSE [splits, S, H] f32, merged
+// by their LSE in the step after attention) and post (the same LSE combine
+// across ranks):
 //   LSE = ln sum_k exp(lse_k);  latent = sum_k exp(lse_k - LSE) o_k,
 // skipping splits whose lse is -inf (their o is never read).
 //
