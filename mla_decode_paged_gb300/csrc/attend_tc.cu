@@ -207,12 +207,12 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Sums over the warp's 32 lanes of each of a lane's C values, by a
-// transposing butterfly: while C is even, a step exchanges half of the
-// values with the partner lane and keeps the sums of the other half, so
-// later steps move fewer values.  On return a lane holds colsum_count(C)
-// sums, of columns base + [0, count); lanes that differ only in the bits
-// colsum_dup(C) hold the same sums.
+// Sums (MAX: maxima) over the warp's 32 lanes of each of a lane's C
+// values, by a transposing butterfly: while C is even, a step exchanges half
+// of the values with the partner lane and keeps the combination of the other
+// half, so later steps move fewer values.  On return a lane holds
+// colsum_count(C) results, of columns base + [0, count); lanes that differ
+// only in the bits colsum_dup(C) hold the same results.
 __host__ __device__ constexpr int colsum_count(int c) {
     for (int d = 16; d >= 1; d >>= 1)
         if (c % 2 == 0) c /= 2;
@@ -226,7 +226,7 @@ __host__ __device__ constexpr int colsum_dup(int c) {
     }
     return m;
 }
-template <int C, int D>
+template <int C, int D, bool MAX = false>
 __device__ __forceinline__ void colsum(float *v, int lane, int &base) {
     if constexpr (D >= 1) {
         if constexpr (C % 2 == 0) {
@@ -235,14 +235,18 @@ __device__ __forceinline__ void colsum(float *v, int lane, int &base) {
             for (int i = 0; i < C / 2; ++i) {
                 const float send = up ? v[i] : v[C / 2 + i];
                 const float keep = up ? v[C / 2 + i] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, D);
+                const float got = __shfl_xor_sync(0xffffffffu, send, D);
+                v[i] = MAX ? fmaxf(keep, got) : keep + got;
             }
             if (up) base += C / 2;
-            colsum<C / 2, D / 2>(v, lane, base);
+            colsum<C / 2, D / 2, MAX>(v, lane, base);
         } else {
 #pragma unroll
-            for (int i = 0; i < C; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], D);
-            colsum<C, D / 2>(v, lane, base);
+            for (int i = 0; i < C; ++i) {
+                const float got = __shfl_xor_sync(0xffffffffu, v[i], D);
+                v[i] = MAX ? fmaxf(v[i], got) : v[i] + got;
+            }
+            colsum<C, D / 2, MAX>(v, lane, base);
         }
     }
 }
@@ -817,12 +821,17 @@ __device__ void softmax(const PP &P, uint8_t *sm) {
         // within the warpgroup.
         const bool g1 = warp >= 4;
         if (g1 ? tc::bar_any(kGroupBar + 1, 128, over) : tc::bar_any(kGroupBar, 128, over)) {
+            {
+                // per-warp column maxima (transposing butterfly)
+                float v[H2];
 #pragma unroll
-            for (int j = 0; j < H2; ++j) {
-                float v = sc[j];
+                for (int j = 0; j < H2; ++j) v[j] = sc[j];
+                int cb = 0;
+                colsum<H2, 16, true>(v, lane, cb);
+                if ((lane & colsum_dup(H2)) == 0) {
 #pragma unroll
-                for (int dd = 16; dd; dd >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, dd));
-                if (lane == 0) ms.red[wq][n0 + j] = v;
+                    for (int i = 0; i < colsum_count(H2); ++i) ms.red[wq][n0 + cb + i] = v[i];
+                }
             }
             if (g1) named_sync(kGroupBar + 1, 128);
             else named_sync(kGroupBar, 128);
