@@ -176,13 +176,18 @@ mla_status mla_decode_attend_paged(const void *q, int64_t q_row_stride, const vo
  * into groups of at most 48) it fills G / g virtual CTAs and gives virtual
  * CTA v's list to CTAs v * g + j, row group j.
  *
- * Layout (int32): plan = [G, offsets[0 .. G], items...], CTA b takes items
- * offsets[b] .. offsets[b + 1] - 1, each MLA_PLAN_ITEM_WORDS int32
+ * Layout (int32): plan = [G, offsets[0 .. G], items..., first[0 .. G-1]],
+ * CTA b takes items offsets[b] .. offsets[b + 1] - 1, each
+ * MLA_PLAN_ITEM_WORDS int32
  *   { r, k | n_r << 9 | group << 18, start, count }:
  * split k (0-based) of the n_r splits of request r covers its tokens
  * [start, start + count) for query-row group `group`; the splits of a
  * request are consecutive ranges that cover all its tokens (an empty
- * request has one split of count 0).
+ * request has one split of count 0).  first[b] repeats CTA b's first item
+ * (zeros for a CTA without items): the kernel starts a CTA from this copy,
+ * which it finds from the plan's length alone, so the offsets and the first
+ * item cost one round trip of loads instead of two.  A plan whose copies
+ * differ from the items is not one this routine writes.
  *
  *   host_lengths  int32 [num_requests], host: tokens per request (<= 0: empty).
  *   num_splits    most splits of one request (the partial buffers' split

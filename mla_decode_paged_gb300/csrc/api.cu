@@ -465,7 +465,8 @@ int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_le
             items += groups;
         }
     if (splits_used) *splits_used = used;
-    const int64_t need = 2 + (int64_t)sm_count + (int64_t)MLA_PLAN_ITEM_WORDS * items;
+    // header, items, then each CTA's first item again (zeros for a CTA with none)
+    const int64_t need = 2 + (int64_t)sm_count + (int64_t)MLA_PLAN_ITEM_WORDS * (items + sm_count);
     if (!plan) return need;
     if (plan_capacity < need) return fail(MLA_ERR_INVALID, "plan buffer too small");
     plan[0] = sm_count;
@@ -485,6 +486,15 @@ int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_le
         }
     }
     plan[1 + sm_count] = (int32_t)pos;
+    // The first items again, at a place the kernel finds from the plan's
+    // length alone: a CTA loads its offsets and its first item at once.
+    int32_t *first = plan + 2 + sm_count + (int64_t)MLA_PLAN_ITEM_WORDS * items;
+    for (int b = 0; b < sm_count; ++b) {
+        const int32_t a = plan[1 + b], e = plan[2 + b];
+        for (int w = 0; w < MLA_PLAN_ITEM_WORDS; ++w)
+            first[(int64_t)MLA_PLAN_ITEM_WORDS * b + w] =
+                a < e ? plan[2 + sm_count + (int64_t)MLA_PLAN_ITEM_WORDS * a + w] : 0;
+    }
     return need;
 }
 

@@ -367,7 +367,8 @@ struct TileIter {
     long long u;
     int t, ntiles, start, count, r, k, n_r, base, grp;
     bool have_unit;
-    int plan_pos, plan_end;      // plan_end < 0: round robin
+    int plan_pos, plan_end;      // plan_end: -1 round robin, -2 a plan not opened yet
+    int plan_items;              // items in the plan (from its length)
 
     int row_groups;
     __device__ void init(const int32_t *indptr, int R, int64_t num_pages, int num_splits, int split_tokens,
@@ -380,28 +381,42 @@ struct TileIter {
         plan_pos = 0;
         plan_end = -1;
         if (plan) {
-            // A plan for another grid, or offsets outside the buffer: flagged, no work.
-            plan_end = 0;
-            const int64_t items = (plan_len - 2 - (int64_t)gridDim.x) / kPlanItemWords;
-            if (plan_len < 2 + (int64_t)gridDim.x || __ldg(plan) != (int)gridDim.x) {
-                flag(MLA_DEV_BAD_PLAN);
-            } else {
-                const int a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
-                if (a < 0 || b < a || (int64_t)b > items) flag(MLA_DEV_BAD_PLAN);
-                else {
-                    plan_pos = a;
-                    plan_end = b;
-                }
-            }
+            plan_end = -2;
+            const int64_t items = (plan_len - 2 - (int64_t)gridDim.x) / kPlanItemWords - (int64_t)gridDim.x;
+            plan_items = items < 0 ? -1 : (int)min(items, (int64_t)INT32_MAX);
         }
     }
 
     // The next plan item into (r, k, n_r, grp, start, count, base); false at
     // the end of the list or on an item that does not fit (flagged).
     __device__ bool plan_next(const int32_t *plan) {
-        if (plan_pos >= plan_end) return false;
-        const int32_t *it = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * plan_pos++;
-        const int ir = __ldg(it), w = __ldg(it + 1), s0 = __ldg(it + 2), c = __ldg(it + 3);
+        int ir, w, s0, c;
+        if (plan_end == -2) {
+            // Opening the plan: the grid check, this CTA's offsets and the copy
+            // of its first item (after the items) are independent loads, one
+            // round trip.  A plan for another grid, or offsets outside the
+            // buffer: flagged, no work.
+            plan_end = 0;
+            if (plan_items < 0) {
+                flag(MLA_DEV_BAD_PLAN);
+                return false;
+            }
+            const int32_t *fi = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * ((int64_t)plan_items + blockIdx.x);
+            const int g0 = __ldg(plan), a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
+            ir = __ldg(fi); w = __ldg(fi + 1); s0 = __ldg(fi + 2); c = __ldg(fi + 3);
+            if (g0 != (int)gridDim.x || a < 0 || b < a || b > plan_items) {
+                flag(MLA_DEV_BAD_PLAN);
+                return false;
+            }
+            plan_pos = a;
+            plan_end = b;
+            if (plan_pos >= plan_end) return false;
+            ++plan_pos;
+        } else {
+            if (plan_pos >= plan_end) return false;
+            const int32_t *it = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * plan_pos++;
+            ir = __ldg(it); w = __ldg(it + 1); s0 = __ldg(it + 2); c = __ldg(it + 3);
+        }
         const int ik = w & 511, inr = (w >> 9) & 511, ig = (w >> 18) & 8191;
         bool ok = w >= 0 && ir >= 0 && ir < cur.R && inr >= 1 && inr <= cur.num_splits && ik < inr &&
                   ig < row_groups && s0 >= 0 && c >= 0;
@@ -427,7 +442,7 @@ struct TileIter {
         Tile T;
         T.valid = false;
         if (!have_unit || t >= ntiles) {
-            if (plan_end >= 0) {
+            if (plan_end != -1) {
                 if (!plan_next(plan)) {
                     have_unit = false;
                     return T;

@@ -7,11 +7,17 @@ ITEM_WORDS = 4
 
 
 def items(plan):
-    """(G, offsets, items [n, 6] = r, k, n_r, group, start, count)."""
+    """(G, offsets, items [n, 6] = r, k, n_r, group, start, count).  The
+    plan ends with a copy of each CTA's first item (G x ITEM_WORDS words,
+    zeros for a CTA without items); it is checked against the items."""
     p = np.asarray(plan, dtype=np.int64)
     G = int(p[0])
     off = p[1:G + 2]
-    raw = p[G + 2:].reshape(-1, ITEM_WORDS)
+    raw = p[G + 2:p.size - ITEM_WORDS * G].reshape(-1, ITEM_WORDS)
+    first = p[p.size - ITEM_WORDS * G:].reshape(G, ITEM_WORDS)
+    for b in range(G):
+        want = raw[off[b]] if off[b] < off[b + 1] else np.zeros(ITEM_WORDS, dtype=np.int64)
+        assert np.array_equal(first[b], want), "first-item copy of CTA %d" % b
     w = raw[:, 1]
     dec = np.stack([raw[:, 0], w & 511, (w >> 9) & 511, (w >> 18) & 8191, raw[:, 2], raw[:, 3]], axis=1)
     return G, off, dec

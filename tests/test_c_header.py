@@ -68,7 +68,9 @@ def test_c_program_calls_the_host_entry_points(tmp_path):
     assert lines[0].startswith("version ") and "sm_103a" in lines[0]
     assert lines[1] == "invalid invalid argument"
     assert lines[2] == "merge %d" % mla.MLA_ERR_INVALID
-    # [256, 128, 1] tokens on 2 CTAs: request 0 alone, then requests 1 and 2 (budget 30 tenths of a tile)
+    # [256, 128, 1] tokens on 2 CTAs: request 0 alone, then requests 1 and 2 (budget 30 tenths of a
+    # tile); then each CTA's first item again
     one = 1 << 9
-    assert lines[3] == "plan 16 used 1: " + " ".join(str(x) for x in
-                                                   [2, 0, 1, 3, 0, one, 0, 256, 1, one, 0, 128, 2, one, 0, 1])
+    assert lines[3] == "plan 24 used 1: " + " ".join(str(x) for x in
+                                                   [2, 0, 1, 3, 0, one, 0, 256, 1, one, 0, 128, 2, one, 0, 1,
+                                                    0, one, 0, 256, 1, one, 0, 128])

@@ -142,6 +142,11 @@ def _first_item(plan):
     return 2 + G      # word index of item 0 (CTA 0's first item)
 
 
+def _first_copy(plan):
+    G = int(plan[0])
+    return plan.numel() - 4 * G   # word index of the copy of CTA 0's first item
+
+
 def _expect_flag(inp, bad):
     _attend(inp, 4, bad)
     assert mla.device_status() & mla.DEV_BAD_PLAN
@@ -159,7 +164,7 @@ def test_plan_offsets_outside_the_buffer_are_flagged():
     inp, plan = _small()
     G = int(plan[0])
     bad = plan.clone()
-    bad[1 + G] = (plan.numel() - 2 - G) // 4 + 1      # the last CTA's list runs past the items
+    bad[1 + G] = (plan.numel() - 2 - G) // 4 - G + 1      # the last CTA's list runs past the items
     _expect_flag(inp, bad)
 
 
@@ -175,9 +180,10 @@ def test_plan_offsets_outside_the_buffer_are_flagged():
 ])
 def test_plan_items_outside_the_launch_are_flagged(field, value):
     inp, plan = _small()
-    w = _first_item(plan) + {"r": 0, "k": 1, "start": 2, "count": 3}[field]
+    off = {"r": 0, "k": 1, "start": 2, "count": 3}[field]
     bad = plan.clone()
-    bad[w] = value
+    bad[_first_item(plan) + off] = value      # the item and the copy the kernel starts from
+    bad[_first_copy(plan) + off] = value
     _expect_flag(inp, bad)
 
 

@@ -60,7 +60,7 @@ def test_plan_structure(lengths, qlen, heads, ns, G):
     g = _groups(qlen, heads)
     Gp, off, it = _plan.items(plan)
     assert Gp == G and plan.dtype == torch.int32
-    assert plan.numel() == 2 + G + _plan.ITEM_WORDS * it.shape[0]
+    assert plan.numel() == 2 + G + _plan.ITEM_WORDS * (it.shape[0] + G)
     assert off[0] == 0 and off[-1] == it.shape[0] and np.all(np.diff(off) >= 0)
     V = G // g
     for b in range(G):
@@ -101,10 +101,12 @@ def test_plan_balance_within_a_tile_of_the_mean(lengths, qlen, heads, ns, G):
 
 def test_plan_by_hand_without_cuts():
     """[256, 128, 1] tokens on 2 CTAs: costs 25, 15, 15; the smallest budget
-    that fits is 30 (request 0 alone, then requests 1 and 2)."""
+    that fits is 30 (request 0 alone, then requests 1 and 2); then each
+    CTA's first item again."""
     plan, used = mla.plan_units([256, 128, 1], 1, 12, 4, sm_count=2)
     one = 1 << 9
-    assert plan.tolist() == [2, 0, 1, 3, 0, one, 0, 256, 1, one, 0, 128, 2, one, 0, 1]
+    assert plan.tolist() == [2, 0, 1, 3, 0, one, 0, 256, 1, one, 0, 128, 2, one, 0, 1,
+                             0, one, 0, 256, 1, one, 0, 128]
     assert used == 1
 
 
@@ -124,7 +126,7 @@ def test_plan_size_query_and_errors(lib):
     lp = ctypes.c_void_p(lens.data_ptr())
     used = ctypes.c_int(0)
     n = lib.mla_plan_units(2, 1, 12, lp, 4, 10, None, 0, ctypes.byref(used))
-    assert n == 2 + 10 + 4 * 3 and used.value == 2          # the 2-tile request is cut in two
+    assert n == 2 + 10 + 4 * (3 + 10) and used.value == 2   # the 2-tile request is cut in two; 10 first-item copies
     buf = torch.empty(n - 1, dtype=torch.int32)
     assert lib.mla_plan_units(2, 1, 12, lp, 4, 10, ctypes.c_void_p(buf.data_ptr()), n - 1, None) == mla.MLA_ERR_INVALID
     assert b"too small" in lib.mla_last_error()
