@@ -298,8 +298,25 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
             rows[i] = r;
         }
     };
-    Tile cur = iter.next(lane, P.plan);
-    if (pw == 0 && lane == 0) {
+    // The first unit for the softmax warps' query preparation.  With a plan
+    // it is published as soon as the first item is read (its request and row
+    // group checked against the launch here; its token range, which needs
+    // the request's page offsets, by next()), one round of loads earlier.
+    int fi[4] = {0, 0, 0, 0};
+    bool early = false;
+    if (P.plan) {
+        early = iter.open_plan(P.plan, fi);
+        const int ig = (fi[1] >> 18) & 8191;
+        early = early && fi[1] >= 0 && fi[0] >= 0 && fi[0] < P.R && ig < P.row_groups && fi[3] >= 0;
+        if (early && pw == 0 && lane == 0) {
+            ms.first[0] = fi[0];
+            ms.first[1] = min(C::T, fi[3]);
+            ms.first[2] = kTileFirst | (ig << 8);
+            mbar_arrive(&ms.first_ready);
+        }
+    }
+    Tile cur = iter.next(lane, P.plan, P.plan ? fi : nullptr);
+    if (!early && pw == 0 && lane == 0) {
         ms.first[0] = cur.r;
         ms.first[1] = cur.ntok;
         ms.first[2] = cur.valid ? cur.flags : kMetaDone;

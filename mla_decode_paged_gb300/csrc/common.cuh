@@ -389,33 +389,49 @@ struct TileIter {
 
     // The next plan item into (r, k, n_r, grp, start, count, base); false at
     // the end of the list or on an item that does not fit (flagged).
-    __device__ bool plan_next(const int32_t *plan) {
+    // Opening the plan: the grid check, this CTA's offsets and the copy of
+    // its first item (after the items) are independent loads, one round
+    // trip; item[] gets the first item's words.  A plan for another grid, or
+    // offsets outside the buffer: flagged, no work.  False when the list is
+    // empty or flagged.
+    __device__ bool open_plan(const int32_t *plan, int (&item)[4]) {
+        plan_end = 0;
+        if (plan_items < 0) {
+            flag(MLA_DEV_BAD_PLAN);
+            return false;
+        }
+        const int32_t *fi = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * ((int64_t)plan_items + blockIdx.x);
+        const int g0 = __ldg(plan), a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) item[i] = __ldg(fi + i);
+        if (g0 != (int)gridDim.x || a < 0 || b < a || b > plan_items) {
+            flag(MLA_DEV_BAD_PLAN);
+            return false;
+        }
+        plan_pos = a;
+        plan_end = b;
+        return a < b;
+    }
+
+    // The next plan item into (r, k, n_r, grp, start, count, base); false at
+    // the end of the list or on an item that does not fit (flagged).  `first`:
+    // the words open_plan returned, for the list's first item.
+    __device__ bool plan_next(const int32_t *plan, const int *first = nullptr) {
         int ir, w, s0, c;
         if (plan_end == -2) {
-            // Opening the plan: the grid check, this CTA's offsets and the copy
-            // of its first item (after the items) are independent loads, one
-            // round trip.  A plan for another grid, or offsets outside the
-            // buffer: flagged, no work.
-            plan_end = 0;
-            if (plan_items < 0) {
-                flag(MLA_DEV_BAD_PLAN);
-                return false;
-            }
-            const int32_t *fi = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * ((int64_t)plan_items + blockIdx.x);
-            const int g0 = __ldg(plan), a = __ldg(plan + 1 + blockIdx.x), b = __ldg(plan + 2 + blockIdx.x);
-            ir = __ldg(fi); w = __ldg(fi + 1); s0 = __ldg(fi + 2); c = __ldg(fi + 3);
-            if (g0 != (int)gridDim.x || a < 0 || b < a || b > plan_items) {
-                flag(MLA_DEV_BAD_PLAN);
-                return false;
-            }
-            plan_pos = a;
-            plan_end = b;
-            if (plan_pos >= plan_end) return false;
+            int item[4];
+            if (!open_plan(plan, item)) return false;
             ++plan_pos;
+            ir = item[0]; w = item[1]; s0 = item[2]; c = item[3];
         } else {
             if (plan_pos >= plan_end) return false;
-            const int32_t *it = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * plan_pos++;
-            ir = __ldg(it); w = __ldg(it + 1); s0 = __ldg(it + 2); c = __ldg(it + 3);
+            if (first) {
+                ++plan_pos;
+                ir = first[0]; w = first[1]; s0 = first[2]; c = first[3];
+            } else {
+                const int32_t *it = plan + 2 + gridDim.x + (int64_t)kPlanItemWords * plan_pos++;
+                ir = __ldg(it); w = __ldg(it + 1); s0 = __ldg(it + 2); c = __ldg(it + 3);
+            }
         }
         const int ik = w & 511, inr = (w >> 9) & 511, ig = (w >> 18) & 8191;
         bool ok = w >= 0 && ir >= 0 && ir < cur.R && inr >= 1 && inr <= cur.num_splits && ik < inr &&
@@ -437,13 +453,14 @@ struct TileIter {
         return true;
     }
 
-    // `plan`: the work plan the iterator was initialised with (or null).
-    __device__ Tile next(int lane, const int32_t *plan = nullptr) {
+    // `plan`: the work plan the iterator was initialised with (or null);
+    // `first`: open_plan's words of the first item, on the first call.
+    __device__ Tile next(int lane, const int32_t *plan = nullptr, const int *first = nullptr) {
         Tile T;
         T.valid = false;
         if (!have_unit || t >= ntiles) {
             if (plan_end != -1) {
-                if (!plan_next(plan)) {
+                if (!plan_next(plan, first)) {
                     have_unit = false;
                     return T;
                 }
