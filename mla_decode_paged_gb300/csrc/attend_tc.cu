@@ -299,12 +299,13 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
         }
     };
     // The first unit for the softmax warps' query preparation.  With a plan
-    // it is published as soon as the first item is read (its request and row
+    // and 32 or 48 query rows (whose preparation the first QK^T waits for) it
+    // is published as soon as the first item is read (its request and row
     // group checked against the launch here; its token range, which needs
     // the request's page offsets, by next()), one round of loads earlier.
     int fi[4] = {0, 0, 0, 0};
     bool early = false;
-    if (P.plan) {
+    if (NQ >= 32 && P.plan) {
         early = iter.open_plan(P.plan, fi);
         const int ig = (fi[1] >> 18) & 8191;
         early = early && fi[1] >= 0 && fi[0] >= 0 && fi[0] < P.R && ig < P.row_groups && fi[3] >= 0;
@@ -315,7 +316,7 @@ __device__ void producer(const PP &P, const CUtensorMap *mlat, const CUtensorMap
             mbar_arrive(&ms.first_ready);
         }
     }
-    Tile cur = iter.next(lane, P.plan, P.plan ? fi : nullptr);
+    Tile cur = iter.next(lane, P.plan, NQ >= 32 && P.plan ? fi : nullptr);
     if (!early && pw == 0 && lane == 0) {
         ms.first[0] = cur.r;
         ms.first[1] = cur.ntok;
