@@ -197,6 +197,8 @@ OTHERS = ("decode_r64_h12", "spec_r128_q4_h12", "long_r32_h96p128")
 # 32 split-KV partials: 32 splits of 512 tokens under the split rule do that
 # for its U[4096, 32768] contexts.
 STATED_CUT = ("spec_r128_q4_h12", (32, 512))
+# ... and the same 8-32 partials per request cut by the balanced host plan.
+STATED_PLAN = (8, 32)   # (min_splits, num_splits)
 
 
 def _parse_splits(text):
@@ -209,11 +211,25 @@ def _parse_splits(text):
     return ns, st
 
 
+def _plan_ranges(plan_h, num_requests):
+    """Per request, its splits' token ranges (row group 0) in a host plan
+    ([G, offsets[G + 1], items of 4 int32, then each CTA's first item again])."""
+    p = plan_h.to(torch.int64).tolist()
+    G = p[0]
+    n_items = p[1 + G]
+    out = [[] for _ in range(num_requests)]
+    for i in range(n_items):
+        r, w, s0, c = p[2 + G + 4 * i: 2 + G + 4 * i + 4]
+        if (w >> 18) & 8191 == 0:
+            out[r].append((s0, s0 + c))
+    return out
+
+
 class Step:
     """One workload's device inputs, split plan, buffers and the step's
     launches (attend, then merge + value/gate)."""
 
-    def __init__(self, spec, args, dev, splits=None):
+    def __init__(self, spec, args, dev, splits=None, plan_splits=None):
         self.spec, self.args, self.dev = spec, args, dev
         splits = splits or _parse_splits(args.splits)
         inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
@@ -228,7 +244,9 @@ class Step:
         # splits the plan used.  A given (num_splits, split_tokens) is timed
         # under the split rule itself.
         self.plan_h = None
-        if not args.no_plan and splits is None:
+        if plan_splits is not None:   # (min_splits, num_splits): a plan honouring a stated partial count
+            self.plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, plan_splits[1], min_splits=plan_splits[0])
+        elif not args.no_plan and splits is None:
             self.plan_h, ns = mla.plan_units(inp.lengths.cpu(), qlen, H, ns)
         self.plan = None if self.plan_h is None else self.plan_h.to(dev)
         self.ns, self.st = ns, st
@@ -481,6 +499,24 @@ def run_gpu(args):
                 per_workload[name]["stated_cut"] = {
                     "num_splits": other.ns, "split_tokens": other.st, "work_plan": "none (split rule)",
                     "partials_per_request": [int(n_r.min()), int(n_r.max())],
+                    "ms_per_step": sum(ts) / len(ts) * 1e3, "tokens_per_s": other.S * len(ts) / sum(ts),
+                    "kernels_us": other.kernels_us(oa, om, ov),
+                    "roofline": {k: rl[k] for k in ("achieved", "frac", "algorithmic_bytes_per_launch")},
+                }
+                # the same partial count from the balanced plan (at least 8 splits a request)
+                del other
+                torch.cuda.empty_cache()
+                other = Step(_spec(name), args, dev, plan_splits=STATED_PLAN)
+                other.warm_and_capture(flush, args.warmup)
+                clocks.mark(True)
+                ts = other.time_graph(flush, args.steps)
+                clocks.mark(False)
+                oa, om, ov = other.time_eager(flush, args.steps)
+                rl = other.roofline(oa)
+                n_r = [len(c) for c in _plan_ranges(other.plan_h, other.spec.requests)]
+                per_workload[name]["stated_cut_planned"] = {
+                    "num_splits": other.ns, "work_plan": "host plan, at least %d splits a request" % STATED_PLAN[0],
+                    "partials_per_request": [min(n_r), max(n_r)],
                     "ms_per_step": sum(ts) / len(ts) * 1e3, "tokens_per_s": other.S * len(ts) / sum(ts),
                     "kernels_us": other.kernels_us(oa, om, ov),
                     "roofline": {k: rl[k] for k in ("achieved", "frac", "algorithmic_bytes_per_launch")},

@@ -209,6 +209,20 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
                        int *splits_used);
 
 /*
+ * mla_plan_units_ex -- mla_plan_units with a floor on the splits per request:
+ * no split of a request takes more than floor(tiles / min_splits) of its
+ * 128-token tiles (at least one, and at least ceil(tiles / num_splits)), so
+ * each request gets at least min_splits splits where its tile count and
+ * num_splits allow; the fill is otherwise the same.  For a workload stated
+ * as "each request split into m..n partials" (min_splits = m, num_splits =
+ * n); min_splits = 1 is mla_plan_units.  1 <= min_splits <= num_splits, else
+ * MLA_ERR_INVALID.
+ */
+int64_t mla_plan_units_ex(int num_requests, int qlen, int heads, const int32_t *host_lengths,
+                          int min_splits, int num_splits, int sm_count, int32_t *plan,
+                          int64_t plan_capacity, int *splits_used);
+
+/*
  * mla_decode_attend_planned -- mla_decode_attend_paged with a work plan.
  *
  * plan (int32 [plan_len], device, 4-byte aligned) as mla_plan_units wrote

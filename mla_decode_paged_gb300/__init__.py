@@ -76,6 +76,8 @@ def library() -> ctypes.CDLL:
                                          vp]
     lib.mla_plan_units.argtypes = [i32, i32, i32, vp, i32, i32, vp, i64, ctypes.POINTER(ctypes.c_int)]
     lib.mla_plan_units.restype = i64
+    lib.mla_plan_units_ex.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, i64, ctypes.POINTER(ctypes.c_int)]
+    lib.mla_plan_units_ex.restype = i64
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.mla_value_gate.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.mla_merge_value_gate.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
@@ -381,25 +383,26 @@ def choose_splits(num_requests, qlen, heads, max_len=0, total_len=0, sm_count=0,
     return int(ns), int(st.value)
 
 
-def plan_units(lengths, qlen, heads, num_splits, sm_count=0):
-    """Balanced host work plan for :func:`attend` (``mla_plan_units``): the
-    requests cut into at most ``num_splits`` splits so that each of
-    ``sm_count`` CTAs (0: the current device's SMs) gets about the same
-    number of tiles.  Returns ``(plan, splits_used)``: a CPU int32 tensor
-    (copy it to the device and pass it as ``attend(..., plan=)``) and the
-    most splits any request got (the smallest ``num_splits`` the partial
-    buffers need)."""
+def plan_units(lengths, qlen, heads, num_splits, sm_count=0, min_splits=1):
+    """Balanced host work plan for :func:`attend` (``mla_plan_units_ex``):
+    the requests cut into at most ``num_splits`` splits (and, where their
+    tiles allow, at least ``min_splits``) so that each of ``sm_count`` CTAs
+    (0: the current device's SMs) gets about the same number of tiles.
+    Returns ``(plan, splits_used)``: a CPU int32 tensor (copy it to the
+    device and pass it as ``attend(..., plan=)``) and the most splits any
+    request got (the smallest ``num_splits`` the partial buffers need)."""
     host = torch.as_tensor(lengths, dtype=torch.int32, device="cpu").contiguous()
     lib = library()
     used = ctypes.c_int(0)
-    args = (host.numel(), int(qlen), int(heads), ctypes.c_void_p(host.data_ptr()), int(num_splits), int(sm_count))
-    n = lib.mla_plan_units(*args, None, 0, ctypes.byref(used))
+    args = (host.numel(), int(qlen), int(heads), ctypes.c_void_p(host.data_ptr()), int(min_splits),
+            int(num_splits), int(sm_count))
+    n = lib.mla_plan_units_ex(*args, None, 0, ctypes.byref(used))
     if n < 0:
-        _check(int(n), "mla_plan_units")
+        _check(int(n), "mla_plan_units_ex")
     plan = torch.empty(n, dtype=torch.int32)
-    n2 = lib.mla_plan_units(*args, ctypes.c_void_p(plan.data_ptr()), n, ctypes.byref(used))
+    n2 = lib.mla_plan_units_ex(*args, ctypes.c_void_p(plan.data_ptr()), n, ctypes.byref(used))
     if n2 < 0:
-        _check(int(n2), "mla_plan_units")
+        _check(int(n2), "mla_plan_units_ex")
     return plan, int(used.value)
 
 

@@ -363,7 +363,15 @@ struct PlanPiece {
 // boundaries where a CTA fills up.  Returns the CTAs used (V + 1 when more
 // than V would be needed or a request would need more than max_splits
 // pieces); pieces are appended per CTA when `out` is given.
-int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_splits, int64_t piece,
+// The most tiles one piece of a request of ntiles tiles may take: so that it
+// gets at least min_splits pieces (one per tile when it has fewer tiles),
+// but never so few tiles that it would need more than max_splits pieces.
+int plan_piece_cap(int ntiles, int min_splits, int max_splits) {
+    const int lo = (ntiles + max_splits - 1) / max_splits;
+    return std::max(ntiles >= min_splits ? ntiles / min_splits : 1, std::max(lo, 1));
+}
+
+int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_splits, int min_splits, int64_t piece,
               std::vector<std::vector<PlanPiece>> *out) {
     int v = 0;
     int64_t load = 0;
@@ -380,6 +388,7 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
             continue;
         }
         const int ntiles = (L + 127) / 128;
+        const int cap = plan_piece_cap(ntiles, min_splits, max_splits);
         int done = 0, k = 0;
         while (done < ntiles) {
             const int64_t room = budget - load;
@@ -391,6 +400,7 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
             int64_t take = (room - piece) / kPlanTile;
             if (take < 1) take = 1;
             if (take > ntiles - done) take = ntiles - done;
+            if (take > cap) take = cap;
             if (++k > max_splits) return V + 1;
             if (out) {
                 const int start = done * 128;
@@ -408,20 +418,27 @@ int plan_fill(const int32_t *lengths, int R, int64_t budget, int V, int max_spli
 
 namespace {
 int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
-                   int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used);
+                   int min_splits, int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used);
 }  // namespace
 
 int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
                        int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
+    return mla_plan_units_ex(num_requests, qlen, heads, host_lengths, 1, num_splits, sm_count, plan, plan_capacity,
+                             splits_used);
+}
+
+int64_t mla_plan_units_ex(int num_requests, int qlen, int heads, const int32_t *host_lengths, int min_splits,
+                          int num_splits, int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
     if (num_requests < 0 || qlen < 1 || qlen > MLA_MAX_QLEN || heads < 1 || heads > MLA_MAX_HEADS ||
         num_splits < 1 || num_splits > MLA_MAX_SPLITS || (num_requests > 0 && !host_lengths))
         return fail(MLA_ERR_INVALID, "bad plan arguments");
+    if (min_splits < 1 || min_splits > num_splits) return fail(MLA_ERR_INVALID, "min_splits outside 1..num_splits");
     if (sm_count <= 0 && (sm_count = device_sms()) <= 0)
         return fail(MLA_ERR_CUDA, "plan_units: no CUDA device to take the SM count from (pass sm_count)");
     if (sm_count > kPlanMaxCtas) return fail(MLA_ERR_INVALID, "sm_count above 65536");
     try {
-        return plan_build(num_requests, qlen, heads, host_lengths, num_splits, sm_count, plan, plan_capacity,
-                          splits_used);
+        return plan_build(num_requests, qlen, heads, host_lengths, num_splits, min_splits, sm_count, plan,
+                          plan_capacity, splits_used);
     } catch (const std::bad_alloc &) {
         return fail(MLA_ERR_INVALID, "host memory for the plan");
     }
@@ -430,7 +447,7 @@ int64_t mla_plan_units(int num_requests, int qlen, int heads, const int32_t *hos
 namespace {
 
 int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_lengths, int num_splits,
-                   int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
+                   int min_splits, int sm_count, int32_t *plan, int64_t plan_capacity, int *splits_used) {
     int groups, nq;
     mla::attend_tc_shape(qlen * heads, &groups, &nq);
     // Each row group of a request runs on its own CTA; the plan fills
@@ -441,19 +458,22 @@ int64_t plan_build(int num_requests, int qlen, int heads, const int32_t *host_le
     if (V < 1) return fail(MLA_ERR_UNSUPPORTED, "fewer SMs than query-row groups");
     const int64_t piece = plan_piece_cost(nq);
     // Smallest budget whose fill fits V CTAs within num_splits pieces per
-    // request (the fill with an unbounded budget always fits: one CTA, one
-    // piece per request).
+    // request (the fill with an unbounded budget always fits: one CTA, the
+    // fewest pieces min_splits allows per request).
     int64_t total = 0;
-    for (int r = 0; r < num_requests; ++r)
-        total += host_lengths[r] > 0 ? ((host_lengths[r] + 127) / 128) * kPlanTile + piece : kPlanEmpty;
+    for (int r = 0; r < num_requests; ++r) {
+        const int t = host_lengths[r] > 0 ? (host_lengths[r] + 127) / 128 : 0;
+        const int cap = plan_piece_cap(t, min_splits, num_splits);
+        total += t > 0 ? (int64_t)t * kPlanTile + (int64_t)((t + cap - 1) / cap) * piece : kPlanEmpty;
+    }
     int64_t lo = 0, hi = total + piece + kPlanTile;
     while (hi - lo > 1) {
         const int64_t mid = lo + (hi - lo) / 2;
-        if (plan_fill(host_lengths, num_requests, mid, V, num_splits, piece, nullptr) <= V) hi = mid;
+        if (plan_fill(host_lengths, num_requests, mid, V, num_splits, min_splits, piece, nullptr) <= V) hi = mid;
         else lo = mid;
     }
     std::vector<std::vector<PlanPiece>> vc;
-    plan_fill(host_lengths, num_requests, hi, V, num_splits, piece, &vc);
+    plan_fill(host_lengths, num_requests, hi, V, num_splits, min_splits, piece, &vc);
     // pieces per request (n_r) and the plan's size
     std::vector<int> n_r(num_requests > 0 ? num_requests : 1, 1);
     int64_t items = 0;

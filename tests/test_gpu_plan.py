@@ -88,6 +88,40 @@ def test_planned_small_workloads_match_oracle(idx, lengths, ns):
     assert mla.device_status() == 0
 
 
+@pytest.mark.parametrize("idx,lengths,mn,ns", [
+    (2, [4096, 700, 2000, 129, 0], 8, 32),   # the speculative workload's 8-32 partials
+    (3, [1500, 300], 4, 8),                  # two row groups of 48
+    (1, [1, 17, 128, 129, 300, 1000], 3, 4),
+])
+def test_min_splits_plans_match_oracle(idx, lengths, mn, ns):
+    """mla_plan_units_ex: requests cut into at least min_splits splits (as
+    their tiles allow); every split's partials and the merged rows against
+    the oracle."""
+    inp_cpu = W.make_inputs(idx, "cpu", lengths=lengths)
+    inp = _dev(inp_cpu)
+    plan, used = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, ns, min_splits=mn)
+    assert used <= ns
+    for L, cuts in zip(lengths, _plan.ranges(plan, len(lengths))):
+        assert len(cuts) >= min(mn, -(-L // 128)) or L == 0
+    o, lse = _attend(inp, ns, plan)
+    _check_against_oracle(inp_cpu, o, lse, plan, ns)
+    assert mla.device_status() == 0
+
+
+def test_min_splits_plan_full_size_speculative_workload(capsys):
+    """The speculative workload cut into 8-32 partials per request by a
+    balanced plan (the benchmark's stated cut with a plan): every row."""
+    inp = W.make_inputs(2, DEV)
+    plan, used = mla.plan_units(inp.lengths.cpu(), inp.qlen, inp.heads, 32, min_splits=8)
+    cuts = _plan.ranges(plan, inp.spec.requests)
+    assert min(len(c) for c in cuts) >= 8 and used <= 32
+    latent, lse_m = mla.merge(*_attend(inp, used, plan))
+    torch.cuda.synchronize()
+    ref = F.reference(("plain", 2), inp)
+    F.check_every_row("%s, plan with 8-32 partials" % inp.spec.name, ref, latent, lse_m, capsys=capsys)
+    assert mla.device_status() == 0
+
+
 def test_planned_causal_block_tables_match_oracle():
     inp_cpu = W.make_block_inputs(2, "cpu", page_size=16, lengths=[2, 3, 257, 700])
     inp = _dev(inp_cpu)

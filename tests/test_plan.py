@@ -99,6 +99,50 @@ def test_plan_balance_within_a_tile_of_the_mean(lengths, qlen, heads, ns, G):
     assert max(loads) <= max(sum(loads) / (V - 1), per_split) + TILE + piece
 
 
+@pytest.mark.parametrize("lengths,qlen,heads,mn,ns,G", [
+    ([4096, 30000, 9000, 700, 0, 129] * 20, 4, 12, 8, 32, 152),   # the speculative workload's kind of cut
+    (list(range(1, 3000, 37)), 1, 12, 4, 16, 152),
+    ([12000] * 32, 1, 96, 8, 32, 152),                           # two row groups
+    ([1000, 128, 5], 8, 12, 8, 8, 16),                           # fewer tiles than min_splits
+])
+def test_plan_min_splits(lengths, qlen, heads, mn, ns, G):
+    """mla_plan_units_ex: every request gets at least min(min_splits, its
+    tiles) splits (num_splits allowing) and at most num_splits; the cuts stay
+    tile-aligned and cover the tokens; the busiest CTA stays within a few
+    pieces of the mean."""
+    plan, used = mla.plan_units(lengths, qlen, heads, ns, sm_count=G, min_splits=mn)
+    g = _groups(qlen, heads)
+    for grp in range(g):
+        for L, cuts in zip(lengths, _plan.ranges(plan, len(lengths), grp)):
+            tiles = -(-max(L, 0) // 128)
+            assert cuts[0][0] == 0 and cuts[-1][1] == max(L, 0)
+            assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:])) and all(s % 128 == 0 for s, _ in cuts)
+            assert len(cuts) <= ns
+            if tiles:
+                assert len(cuts) >= min(mn, tiles, ns)
+    V = G // g
+    _, off, it = _plan.items(plan)
+    piece = _piece(qlen, heads)
+    loads = [sum(_cost(c, piece) for c in it[off[v * g]:off[v * g + 1], 5]) for v in range(V)]
+    cap = max(-(-(-(-max(lengths) // 128)) // mn), 1) if lengths else 1
+    assert max(loads) <= sum(loads) / (V - 1) + cap * TILE + 2 * piece
+    assert used == max(len(c) for c in _plan.ranges(plan, len(lengths)))
+
+
+def test_plan_min_splits_one_is_the_plain_plan(lib):
+    lens = [5000, 100, 8000, 1, 0, 4096]
+    a, ua = mla.plan_units(lens, 1, 12, 7, sm_count=152)
+    b, ub = mla.plan_units(lens, 1, 12, 7, sm_count=152, min_splits=1)
+    assert torch.equal(a, b) and ua == ub
+    lt = torch.tensor(lens, dtype=torch.int32)
+    lp = ctypes.c_void_p(lt.data_ptr())
+    n = lib.mla_plan_units(len(lens), 1, 12, lp, 7, 152, None, 0, None)
+    assert n == a.numel()
+    for bad in (0, 8):   # min_splits outside 1..num_splits
+        assert lib.mla_plan_units_ex(len(lens), 1, 12, lp, bad, 7, 152, None, 0, None) == mla.MLA_ERR_INVALID
+        assert b"min_splits" in lib.mla_last_error()
+
+
 def test_plan_by_hand_without_cuts():
     """[256, 128, 1] tokens on 2 CTAs: costs 25, 15, 15; the smallest budget
     that fits is 30 (request 0 alone, then requests 1 and 2); then each
