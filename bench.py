@@ -232,6 +232,8 @@ class Step:
     def __init__(self, spec, args, dev, splits=None, plan_splits=None):
         self.spec, self.args, self.dev = spec, args, dev
         splits = splits or _parse_splits(args.splits)
+        if plan_splits is None and splits is None and getattr(args, "plan_splits", None):
+            plan_splits = _parse_splits(args.plan_splits)
         inp = W.make_inputs(spec, dev) if args.page_size == 1 else W.make_block_inputs(spec, dev, args.page_size)
         self.inp = inp
         self.last = inp.extra.get("last_page_len")
@@ -814,6 +816,8 @@ def main():
                     help="round-robin work units under the split rule instead of the host work plan")
     ap.add_argument("--splits", default=None, metavar="NS:ST",
                     help="num_splits:split_tokens under the split rule (no work plan) instead of the host plan")
+    ap.add_argument("--plan-splits", default=None, metavar="MIN:MAX",
+                    help="host plan with at least MIN and at most MAX splits per request")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     ap.add_argument("--clocks-dir", default=None,
