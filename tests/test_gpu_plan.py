@@ -108,6 +108,17 @@ def test_min_splits_plans_match_oracle(idx, lengths, mn, ns):
     assert mla.device_status() == 0
 
 
+def test_min_splits_plan_causal_block_tables_match_oracle():
+    """A minimum-splits plan with the causal mask over a block-table cache
+    (page size 16): consecutive splits of one request on one CTA."""
+    inp_cpu = W.make_block_inputs(2, "cpu", page_size=16, lengths=[2, 3, 257, 1400, 700])
+    inp = _dev(inp_cpu)
+    plan, used = mla.plan_units(inp_cpu.lengths, inp.qlen, inp.heads, 16, min_splits=6)
+    o, lse = _attend(inp, 16, plan, causal=True)
+    _check_against_oracle(inp_cpu, o, lse, plan, 16, causal=True)
+    assert mla.device_status() == 0
+
+
 def test_min_splits_plan_full_size_speculative_workload(capsys):
     """The speculative workload cut into 8-32 partials per request by a
     balanced plan (the benchmark's stated cut with a plan): every row."""
