@@ -29,6 +29,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -84,9 +85,15 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _spec(name):
+def _spec(name, requests=None):
+    """The named workload; with ``requests`` a smaller case of it (the same
+    shapes and distributions, the first ``requests`` requests drawn), named
+    ``<name>:r<requests>`` (its DRAM traffic is not the full workload's)."""
     for s in W.WORKLOADS:
         if s.name == name:
+            if requests:
+                s = dataclasses.replace(s, name="%s:r%d" % (s.name, requests), requests=requests,
+                                        zero_requests=min(s.zero_requests, requests))
             return s
     raise SystemExit("unknown workload %s (have %s)" % (name, [s.name for s in W.WORKLOADS]))
 
@@ -354,7 +361,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     mla.build()
-    spec = _spec(args.workload)
+    spec = _spec(args.workload, args.requests)
     step = Step(spec, args, dev)
     inp, S, ns, st, plan = step.inp, step.S, step.ns, step.st, step.plan
     R, qlen, H = spec.requests, spec.qlen, spec.heads
@@ -467,7 +474,7 @@ def run_gpu(args):
     # ---- the other full-size workloads, each timed the same way (rank 0 of
     # a single-GPU run only: the scaling runs need the headline alone)
     per_workload = {}
-    if ws == 1 and not args.no_per_workload and args.workload == HEADLINE:
+    if ws == 1 and not args.no_per_workload and args.workload == HEADLINE and args.requests is None:
         for name in OTHERS:
             other = Step(_spec(name), args, dev)
             other.warm_and_capture(flush, args.warmup)
@@ -771,7 +778,7 @@ def run_reference(args):
     ws, rank, local = _dist()
     if rank != 0:
         return None
-    spec = _spec(args.workload)
+    spec = _spec(args.workload, args.requests)
     inp = W.make_inputs(spec, "cpu")
     times = []
     base = None
@@ -818,6 +825,8 @@ def main():
                     help="num_splits:split_tokens under the split rule (no work plan) instead of the host plan")
     ap.add_argument("--plan-splits", default=None, metavar="MIN:MAX",
                     help="host plan with at least MIN and at most MAX splits per request")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="a smaller case of the workload: its first N requests (for profiling captures)")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask within a request (row tq sees its first L - qlen + tq + 1 tokens)")
     ap.add_argument("--clocks-dir", default=None,
@@ -825,6 +834,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.requests is not None and args.requests < 1:
+        raise SystemExit("--requests must be at least 1")
     rec = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if rec is not None:
         print(json.dumps(rec), flush=True)

@@ -106,3 +106,18 @@ def test_clocks_without_nvidia_smi_say_so(tmp_path):
     c = bench.Clocks(0, str(tmp_path))
     c.proc = None
     assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_smaller_case_of_a_workload():
+    """--requests N: the same workload's shapes and distributions with N
+    requests, under its own name (so no full-size ncu traffic is taken for
+    it); without it the workload as stated."""
+    full = bench._spec("ragged_r256_q8_h12")
+    small = bench._spec("ragged_r256_q8_h12", 64)
+    assert full.requests == 256 and full.name == "ragged_r256_q8_h12"
+    assert small.requests == 64 and small.name == "ragged_r256_q8_h12:r64"
+    assert (small.qlen, small.heads, small.lengths, small.kv_scale, small.seed) == \
+        (full.qlen, full.heads, full.lengths, full.kv_scale, full.seed)
+    assert small.zero_requests == full.zero_requests
+    assert bench._spec("ragged_r256_q8_h12", 4).zero_requests == 4
+    assert bench._ncu_traffic(small.name) is None
