@@ -81,6 +81,31 @@ def test_kv_append_bit_exact(T, pool, k_scale):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("k_scale", [1.0, 0.8, 1.25, 1.0 / 3.0, 448.0, 2.0 ** -10])
+def test_kv_append_every_bf16_value(k_scale):
+    """Every bf16 bit pattern (zeros, subnormals, normals, infinities, NaNs
+    of both signs) through the append, against the oracle's IEEE float32
+    quotient and e4m3 rounding: 65,536 values as 114 tokens (the last one
+    padded with zeros), in two halves of the kernel's units (kv_c and k_pe)."""
+    T, pool = 114, 300
+    codes = torch.arange(65536, dtype=torch.int32)
+    vals = torch.zeros(T * 576, dtype=torch.int32)
+    vals[:65536] = codes
+    rows = vals.view(T, 576).to(torch.int16).view(torch.bfloat16)
+    kv_c, k_pe = rows[:, :512].contiguous(), rows[:, 512:].contiguous()
+    g = torch.Generator().manual_seed(3)
+    kv0 = torch.randint(0, 256, (pool, 576), generator=g, dtype=torch.uint8)
+    slots = torch.randperm(pool, generator=g)[:T].to(torch.int64)
+    kv = kv0.cuda()
+    mla.kv_append(kv, kv_c.cuda(), k_pe.cuda(), slots.cuda(), k_scale)
+    torch.cuda.synchronize()
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns widened by numpy
+        ref = O.kv_append(u8(kv0), bf16_bits(kv_c), bf16_bits(k_pe), slots.numpy(), k_scale)
+    assert np.array_equal(u8(kv), ref)
+    assert mla.device_status() == 0
+
+
+@pytest.mark.gpu
 def test_kv_append_strided_rows_and_bad_slots_flagged():
     T, pool = 64, 100
     big = torch.randn(T, 1024).to(torch.bfloat16)        # kv_c and k_pe as column views of wider rows
