@@ -33,7 +33,7 @@ cudaError_t merge_launch(const void *o, const float *lse, int num_splits, int ro
                          void *latent, float *lse_out, cudaStream_t st);
 cudaError_t merge_status(unsigned int *flags, bool clear);
 cudaError_t value_gate_launch(const void *latent, const void *w_uv, const void *gate,
-                              const int32_t *lengths, int R, int qlen, int H, void *out, cudaStream_t st);
+                              const int32_t *lengths, int R, int qlen, int H, void *out, int sms, cudaStream_t st);
 cudaError_t value_gate_status(unsigned int *flags, bool clear);
 cudaError_t merge_value_launch(const void *o, const float *lse, int num_splits, const void *w_uv, const void *gate,
                                const int32_t *lengths, int R, int qlen, int H, void *out, void *latent,
@@ -225,7 +225,9 @@ mla_status mla_value_gate(const void *latent, const void *w_uv, const void *gate
         !aligned(lengths, 4))
         return fail(MLA_ERR_INVALID, "misaligned pointer (latent, w_uv need 16 bytes)");
     if ((int64_t)num_requests * qlen > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
-    cudaError_t e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out,
+    const int sms = device_sms();
+    if (sms <= 0) return fail(MLA_ERR_CUDA, "no CUDA device");
+    cudaError_t e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out, sms,
                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "value_gate launch");
     return MLA_OK;
@@ -251,7 +253,7 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     cudaError_t e;
     // One launch while its 16-row CTAs (one per SM at a time) number at most
     // two waves; past that, loading the head's 128 KB W_UV slice per 16 rows
-    // costs more than the separate merge and the 64-row value kernel save.
+    // costs more than the separate merge and the 64- or 96-row value kernel save.
     // Graph-replayed steps on one GB300: 64 x 12 rows (48 CTAs) and 32 x 96
     // (192) are faster fused, 512 x 12 (384) and 2,048 x 12 (1,536) split.
     if (((S + 15) / 16) * heads <= 2 * (int64_t)sms) {
@@ -260,7 +262,7 @@ mla_status mla_merge_value_gate(const void *o, const float *lse, int num_splits,
     } else {
         e = mla::merge_launch(o, lse, num_splits, (int)S, heads, latent, lse_out, st);
         if (e == cudaSuccess)
-            e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out, st);
+            e = mla::value_gate_launch(latent, w_uv, gate, lengths, num_requests, qlen, heads, out, sms, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "merge_value_gate launch");
     return MLA_OK;
