@@ -224,7 +224,7 @@ def test_merge_standalone(splits, rows, heads):
 
 @pytest.mark.parametrize("R,qlen,heads", [(3, 1, 12), (70, 1, 12), (5, 4, 12), (9, 8, 12), (2, 1, 96), (1, 3, 5),
                                           (33, 4, 12), (3, 1, 128), (40, 5, 3),
-                                          # the persistent kernel: several 32-row tiles per CTA, ragged last tile
+                                          # 2,000 x 12 rows: 96-row tiles on a 152-SM GB300, ragged last tile
                                           (250, 8, 12), (45, 3, 64), (1100, 1, 12)])
 def test_value_gate_standalone(R, qlen, heads):
     S = R * qlen
@@ -241,6 +241,24 @@ def test_value_gate_standalone(R, qlen, heads):
     assert_bf16_close(out, ref, "value_gate")
     dead = np.repeat(lengths.numpy() == 0, qlen)
     assert torch.all(out[torch.from_numpy(dead).to(DEV)] == 0)
+
+
+def test_value_gate_tile_height_does_not_change_bytes():
+    """2,000 rows x 12 heads in one call take 96-row tiles (64-row ones would
+    be more than two waves of CTAs on a 152-SM GB300); the same rows as two
+    calls of 1,000 take 64-row tiles.  Each row gets the same MMAs in the same
+    K order and the same epilogue, so the outputs are byte-equal."""
+    S, H = 2000, 12
+    lat = W.make_latent(S, H, seed=9).to(DEV)
+    g = torch.Generator().manual_seed(9)
+    w = (torch.randn(H, 128, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16).to(DEV)
+    gate = torch.randn(S, H * 128, generator=g).to(torch.bfloat16).to(DEV)
+    lengths = torch.randint(0, 3, (S,), generator=g, dtype=torch.int32).to(DEV)
+    whole = mla.value_gate(lat, w, gate, lengths, 1)
+    first = mla.value_gate(lat[:1000], w, gate[:1000], lengths[:1000], 1)
+    second = mla.value_gate(lat[1000:], w, gate[1000:], lengths[1000:], 1)
+    assert torch.equal(whole, torch.cat([first, second]))
+    assert mla.device_status() == 0
 
 
 @pytest.mark.parametrize("idx,lengths", SMALL)
